@@ -1,0 +1,421 @@
+// libadaln C-ABI: argument checks, launch planning and launches. See include/adaln.h.
+#include "adaln.h"
+
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "launch.h"
+
+using namespace adaln;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+int g_sms[kMaxDevices];  // 0 = not yet queried
+std::map<std::tuple<int, int, int, int, int, int>, int> g_occupancy;
+
+// Multiprocessor count of the current device (cached), or 0 on failure.
+int current_sms(int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    *dev_out = dev;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_sms[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_sms[dev] = sms;
+    }
+    return g_sms[dev];
+}
+
+// How a row of width D is spread over a CTA: each thread owns `nv` 16-byte vectors
+// (v = tid + k * tpb), so a CTA holds one row in registers.
+struct RowCfg {
+    int nv;
+    int tpb;
+};
+
+RowCfg row_cfg(int64_t D, adaln_dtype dtype) {
+    const int64_t VE = dtype == ADALN_BF16 ? 8 : 4;
+    const int64_t V = D / VE;
+    int64_t nv = (V + 511) / 512;
+    if (nv < 1) nv = 1;
+    if (nv > 4) nv = 4;
+    const int64_t per = (V + nv - 1) / nv;
+    return RowCfg{(int)nv, (int)((per + 31) / 32 * 32)};
+}
+
+enum Kind { kFwd = 0, kBwd = 1 };
+
+// Row tiles of one launch: every resident CTA slot of the device, at most one per row.
+int64_t plan_tiles(Kind kind, adaln_dtype dtype, const RowCfg& c, bool varlen, int64_t R,
+                   int* sms_out) {
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    if (sms <= 0) return -1;
+    *sms_out = sms;
+    const auto key = std::make_tuple(dev, (int)kind, (int)dtype, c.nv, (int)varlen, c.tpb);
+    int bps = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_occupancy.find(key);
+        if (it != g_occupancy.end()) bps = it->second;
+    }
+    if (bps == 0) {
+        const cudaError_t e = kind == kFwd ? fwd_blocks_per_sm((int)dtype, c.nv, varlen, c.tpb, &bps)
+                                           : bwd_blocks_per_sm((int)dtype, c.nv, varlen, c.tpb, &bps);
+        if (e != cudaSuccess || bps <= 0) return -1;
+        std::lock_guard<std::mutex> lock(g_mu);
+        g_occupancy[key] = bps;
+    }
+    int64_t G = (int64_t)sms * bps;
+    if (G > kMaxCtas) G = kMaxCtas;
+    if (G > R) G = R;
+    if (G < 1) G = 1;
+    return G;
+}
+
+// float4 columns per stage-2 CTA: aim for ~4 CTAs per SM over all modulation rows.
+int stage2_cw(int64_t D, int64_t nmod, int sms) {
+    const int64_t D4 = D / 4;
+    const int64_t target = 4 * (int64_t)sms;
+    const int64_t ranges = (target + nmod - 1) / (nmod > 0 ? nmod : 1);
+    const int64_t per = (D4 + ranges - 1) / ranges;
+    int cw = 1;
+    while ((int64_t)cw * 2 <= per && cw * 2 <= kStage2Threads) cw *= 2;
+    return cw;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(int64_t D, adaln_dtype dtype) {
+    if (dtype != ADALN_F32 && dtype != ADALN_BF16) return ADALN_ERR_INVALID_ARG;
+    if (D < 8 || D > 16384 || D % 8 != 0) return ADALN_ERR_UNSUPPORTED;
+    return ADALN_OK;
+}
+
+bool rows_fit(int64_t R, int64_t D) { return R >= 0 && R <= (INT64_MAX / 16) / D; }
+
+// Row tensors and modulation tables: present and 16-byte aligned.
+int check_io(std::initializer_list<const void*> vecs, std::initializer_list<const void*> stats) {
+    for (const void* p : vecs) {
+        if (!p) return ADALN_ERR_INVALID_ARG;
+        if (!aligned(p, 16)) return ADALN_ERR_ALIGNMENT;
+    }
+    for (const void* p : stats) {
+        if (!p) return ADALN_ERR_INVALID_ARG;
+        if (!aligned(p, 4)) return ADALN_ERR_ALIGNMENT;
+    }
+    return ADALN_OK;
+}
+
+int check_workspace(const void* ws, size_t bytes, size_t need) {
+    if (!ws) return ADALN_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return ADALN_ERR_ALIGNMENT;
+    if (bytes < need) return ADALN_ERR_WORKSPACE;
+    return ADALN_OK;
+}
+
+size_t bwd_need(int64_t G, int64_t nseg, int64_t D) {
+    return kPartialsOffset + (size_t)(G + nseg) * 2 * (size_t)D * sizeof(float);
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? ADALN_OK : ADALN_ERR_CUDA; }
+
+Segments dense_segments(int64_t Bt, int64_t N) {
+    return Segments{nullptr, nullptr, Bt, N, Bt, Bt * N};
+}
+
+Segments packed_segments(const int32_t* cu, const int32_t* mod, int32_t nseg, int64_t total,
+                         int64_t nmod) {
+    return Segments{cu, mod, nseg, 0, nmod, total};
+}
+
+// ---- shared bodies of the dense and packed calls -----------------------------------------
+
+int run_fwd(const void* x, const void* shift, const void* scale, void* y, float* mean,
+            float* rstd, const Segments& seg, int64_t D, float eps, void* ws, bool varlen,
+            adaln_dtype dtype, cudaStream_t stream) {
+    const RowCfg c = row_cfg(D, dtype);
+    int sms = 0;
+    const int64_t G = plan_tiles(kFwd, dtype, c, varlen, seg.R, &sms);
+    if (G < 0) return ADALN_ERR_CUDA;
+    FwdArgs a{};
+    a.x = x;
+    a.shift = shift;
+    a.scale = scale;
+    a.y = y;
+    a.mean = mean;
+    a.rstd = rstd;
+    a.D = D;
+    a.eps = eps;
+    a.seg = seg;
+    a.status = ws ? reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kHeaderBytes) : nullptr;
+    a.header = static_cast<WsHeader*>(ws);
+    return launched(launch_fwd(a, (int)dtype, c.nv, varlen, G, c.tpb, stream));
+}
+
+int64_t bwd_tiles(int64_t R, int64_t D, bool varlen, adaln_dtype dtype, int* sms) {
+    return plan_tiles(kBwd, dtype, row_cfg(D, dtype), varlen, R, sms);
+}
+
+enum Stages { kPartials = 1, kReduce = 2, kBoth = 3 };
+
+int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+            const void* scale, void* dx, float* dshift, float* dscale, const Segments& seg,
+            int64_t D, void* ws, size_t ws_bytes, bool varlen, adaln_dtype dtype,
+            cudaStream_t stream, int stages) {
+    if (int rc = check_workspace(ws, ws_bytes, kPartialsOffset)) return rc;
+    const RowCfg c = row_cfg(D, dtype);
+    int sms = 0;
+    const int64_t G = plan_tiles(kBwd, dtype, c, varlen, seg.R, &sms);
+    if (G < 0) return ADALN_ERR_CUDA;
+    if (int rc = check_workspace(ws, ws_bytes, bwd_need(G, seg.nseg, D))) return rc;
+    char* base = static_cast<char*>(ws);
+    BwdArgs a{};
+    a.dy = dy;
+    a.x = x;
+    a.mean = mean;
+    a.rstd = rstd;
+    a.scale = scale;
+    a.dx = dx;
+    a.partials = reinterpret_cast<float*>(base + kPartialsOffset);
+    a.D = D;
+    a.seg = seg;
+    a.status = reinterpret_cast<uint32_t*>(base + kHeaderBytes);
+    a.header = reinterpret_cast<WsHeader*>(base);
+    if (stages & kPartials) {
+        if (int rc = launched(launch_bwd(a, (int)dtype, c.nv, varlen, G, c.tpb, stream))) return rc;
+    }
+    if (!(stages & kReduce) || seg.nmod == 0) return ADALN_OK;
+    Stage2Args s{};
+    s.partials = a.partials;
+    s.dshift = dshift;
+    s.dscale = dscale;
+    s.D = D;
+    s.G = G;
+    s.cw = stage2_cw(D, seg.nmod, sms);
+    s.seg = seg;
+    return launched(launch_stage2(s, varlen, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int adaln_fwd(const void* x, const void* shift, const void* scale, void* y, float* mean,
+              float* rstd, int64_t Bt, int64_t N, int64_t D, float eps, adaln_dtype dtype,
+              cudaStream_t stream) {
+    if (int rc = check_shape(D, dtype)) return rc;
+    if (Bt < 0 || N < 0 || !(eps > 0.0f) || !std::isfinite(eps)) return ADALN_ERR_INVALID_ARG;
+    if (N > 0 && Bt > INT64_MAX / N) return ADALN_ERR_INVALID_ARG;
+    const int64_t R = Bt * N;
+    if (!rows_fit(R, D)) return ADALN_ERR_INVALID_ARG;
+    if (R == 0) return ADALN_OK;
+    if (int rc = check_io({x, shift, scale, y}, {mean, rstd})) return rc;
+    return run_fwd(x, shift, scale, y, mean, rstd, dense_segments(Bt, N), D, eps, nullptr, false,
+                   dtype, stream);
+}
+
+size_t adaln_bwd_workspace_size(int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype) {
+    if (check_shape(D, dtype) || Bt < 0 || N < 0) return 0;
+    if (N > 0 && Bt > INT64_MAX / N) return 0;
+    int sms = 0;
+    const int64_t G = bwd_tiles(Bt * N, D, false, dtype, &sms);
+    if (G < 0) return 0;
+    return bwd_need(G, Bt, D);
+}
+
+}  // extern "C"
+
+static int bwd_dense(const void* dy, const void* x, const float* mean, const float* rstd,
+              const void* scale, void* dx, float* dshift, float* dscale, void* workspace,
+              size_t workspace_bytes, int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype,
+              cudaStream_t stream, int stages) {
+    if (int rc = check_shape(D, dtype)) return rc;
+    if (Bt < 0 || N < 0) return ADALN_ERR_INVALID_ARG;
+    if (N > 0 && Bt > INT64_MAX / N) return ADALN_ERR_INVALID_ARG;
+    const int64_t R = Bt * N;
+    if (!rows_fit(R, D)) return ADALN_ERR_INVALID_ARG;
+    if (Bt == 0) return ADALN_OK;
+    if (int rc = check_io({dshift, dscale}, {})) return rc;
+    if (R > 0) {
+        if (int rc = check_io({dy, x, scale, dx}, {mean, rstd})) return rc;
+    }
+    return run_bwd(dy, x, mean, rstd, scale, dx, dshift, dscale, dense_segments(Bt, N), D,
+                   workspace, workspace_bytes, false, dtype, stream, stages);
+}
+
+extern "C" {
+
+int adaln_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+              const void* scale, void* dx, float* dshift, float* dscale, void* workspace,
+              size_t workspace_bytes, int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype,
+              cudaStream_t stream) {
+    return bwd_dense(dy, x, mean, rstd, scale, dx, dshift, dscale, workspace, workspace_bytes, Bt, N,
+                     D, dtype, stream, kBoth);
+}
+
+int adaln_bwd_partials(const void* dy, const void* x, const float* mean, const float* rstd,
+                       const void* scale, void* dx, float* dshift, float* dscale, void* workspace,
+                       size_t workspace_bytes, int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype,
+                       cudaStream_t stream) {
+    return bwd_dense(dy, x, mean, rstd, scale, dx, dshift, dscale, workspace, workspace_bytes, Bt, N,
+                     D, dtype, stream, kPartials);
+}
+
+int adaln_bwd_reduce(const void* dy, const void* x, const float* mean, const float* rstd,
+                     const void* scale, void* dx, float* dshift, float* dscale, void* workspace,
+                     size_t workspace_bytes, int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype,
+                     cudaStream_t stream) {
+    return bwd_dense(dy, x, mean, rstd, scale, dx, dshift, dscale, workspace, workspace_bytes, Bt, N,
+                     D, dtype, stream, kReduce);
+}
+
+size_t adaln_fwd_varlen_workspace_size(int64_t total_tokens, int32_t nseg, int64_t D,
+                                       adaln_dtype dtype) {
+    if (check_shape(D, dtype) || total_tokens < 0 || nseg < 0) return 0;
+    return kPartialsOffset;
+}
+
+int adaln_fwd_varlen(const void* x, const void* shift, const void* scale, void* y, float* mean,
+                     float* rstd, const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                     int64_t total_tokens, int64_t nmod, int64_t D, float eps, void* workspace,
+                     size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream) {
+    if (int rc = check_shape(D, dtype)) return rc;
+    if (nseg < 0 || total_tokens < 0 || total_tokens > INT32_MAX || nmod < 0)
+        return ADALN_ERR_INVALID_ARG;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return ADALN_ERR_INVALID_ARG;
+    if (!rows_fit(total_tokens, D) || !rows_fit(nmod, D)) return ADALN_ERR_INVALID_ARG;
+    if (!cu_seqlens || (nseg > 0 && !mod_idx)) return ADALN_ERR_INVALID_ARG;
+    if (nseg == 0 && total_tokens > 0) return ADALN_ERR_INVALID_ARG;
+    if (int rc = check_workspace(workspace, workspace_bytes, kPartialsOffset)) return rc;
+    if (total_tokens > 0) {
+        if (int rc = check_io({x, y}, {mean, rstd})) return rc;
+        if (nmod > 0) {
+            if (int rc = check_io({shift, scale}, {})) return rc;
+        }
+    }
+    return run_fwd(x, shift, scale, y, mean, rstd,
+                   packed_segments(cu_seqlens, mod_idx, nseg, total_tokens, nmod), D, eps,
+                   workspace, true, dtype, stream);
+}
+
+size_t adaln_bwd_varlen_workspace_size(int64_t total_tokens, int32_t nseg, int64_t nmod,
+                                       int64_t D, adaln_dtype dtype) {
+    if (check_shape(D, dtype) || total_tokens < 0 || nseg < 0 || nmod < 0) return 0;
+    int sms = 0;
+    const int64_t G = bwd_tiles(total_tokens, D, true, dtype, &sms);
+    if (G < 0) return 0;
+    return bwd_need(G, nseg, D);
+}
+
+}  // extern "C"
+
+static int bwd_packed(const void* dy, const void* x, const float* mean, const float* rstd,
+                     const void* scale, void* dx, float* dshift, float* dscale,
+                     const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                     int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
+                     size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream, int stages) {
+    if (int rc = check_shape(D, dtype)) return rc;
+    if (nseg < 0 || total_tokens < 0 || total_tokens > INT32_MAX || nmod < 0)
+        return ADALN_ERR_INVALID_ARG;
+    if (!rows_fit(total_tokens, D) || !rows_fit(nmod, D)) return ADALN_ERR_INVALID_ARG;
+    if (!cu_seqlens || (nseg > 0 && !mod_idx)) return ADALN_ERR_INVALID_ARG;
+    if (nseg == 0 && total_tokens > 0) return ADALN_ERR_INVALID_ARG;
+    if (nmod > 0) {
+        if (int rc = check_io({dshift, dscale}, {})) return rc;
+    }
+    if (total_tokens > 0) {
+        if (int rc = check_io({dy, x, dx}, {mean, rstd})) return rc;
+        if (nmod > 0) {
+            if (int rc = check_io({scale}, {})) return rc;
+        }
+    }
+    return run_bwd(dy, x, mean, rstd, scale, dx, dshift, dscale,
+                   packed_segments(cu_seqlens, mod_idx, nseg, total_tokens, nmod), D, workspace,
+                   workspace_bytes, true, dtype, stream, stages);
+}
+
+extern "C" {
+
+int adaln_bwd_varlen(const void* dy, const void* x, const float* mean, const float* rstd,
+                     const void* scale, void* dx, float* dshift, float* dscale,
+                     const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                     int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
+                     size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream) {
+    return bwd_packed(dy, x, mean, rstd, scale, dx, dshift, dscale, cu_seqlens, mod_idx, nseg,
+                      total_tokens, nmod, D, workspace, workspace_bytes, dtype, stream, kBoth);
+}
+
+int adaln_bwd_varlen_partials(const void* dy, const void* x, const float* mean, const float* rstd,
+                     const void* scale, void* dx, float* dshift, float* dscale,
+                     const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                     int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
+                     size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream) {
+    return bwd_packed(dy, x, mean, rstd, scale, dx, dshift, dscale, cu_seqlens, mod_idx, nseg,
+                      total_tokens, nmod, D, workspace, workspace_bytes, dtype, stream, kPartials);
+}
+
+int adaln_bwd_varlen_reduce(const void* dy, const void* x, const float* mean, const float* rstd,
+                     const void* scale, void* dx, float* dshift, float* dscale,
+                     const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                     int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
+                     size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream) {
+    return bwd_packed(dy, x, mean, rstd, scale, dx, dshift, dscale, cu_seqlens, mod_idx, nseg,
+                      total_tokens, nmod, D, workspace, workspace_bytes, dtype, stream, kReduce);
+}
+
+int adaln_read_status(const void* workspace, cudaStream_t stream) {
+    if (!workspace) return ADALN_ERR_WORKSPACE;
+    WsHeader h{};
+    if (cudaMemcpyAsync(&h, workspace, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return ADALN_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ADALN_ERR_CUDA;
+    if (h.magic != kStatusMagic || h.nwords == 0 || h.nwords > (uint32_t)kMaxCtas)
+        return ADALN_ERR_WORKSPACE;
+    std::vector<uint32_t> words(h.nwords);
+    if (cudaMemcpyAsync(words.data(), static_cast<const char*>(workspace) + kHeaderBytes,
+                        sizeof(uint32_t) * words.size(), cudaMemcpyDeviceToHost,
+                        stream) != cudaSuccess)
+        return ADALN_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ADALN_ERR_CUDA;
+    uint32_t all = 0;
+    for (uint32_t w : words) all |= w;
+    if (all & kErrSeqlens) return ADALN_ERR_BAD_SEQLENS;
+    if (all & kErrModIdx) return ADALN_ERR_BAD_MOD_IDX;
+    return ADALN_OK;
+}
+
+int64_t adaln_bucket_batch(int64_t S, int64_t M_mem, int64_t M_comp, int32_t p) {
+    if (S <= 0 || M_mem <= 0 || M_comp <= 0 || p < 1) return -(int64_t)ADALN_ERR_INVALID_ARG;
+    const int64_t by_memory = M_mem / S;
+    // floor(M_comp / S^p) as p nested floor divisions: floor(floor(a/b)/c) == floor(a/(b*c))
+    // for positive integers, so S^p is never formed and nothing can overflow.
+    int64_t by_compute = M_comp;
+    for (int32_t i = 0; i < p && by_compute > 0; ++i) by_compute /= S;
+    const int64_t b = by_memory < by_compute ? by_memory : by_compute;
+    return b > 1 ? b : 1;
+}
+
+const char* adaln_status_string(int status) {
+    switch (status) {
+        case ADALN_OK: return "ADALN_OK";
+        case ADALN_ERR_INVALID_ARG: return "ADALN_ERR_INVALID_ARG: invalid argument";
+        case ADALN_ERR_UNSUPPORTED: return "ADALN_ERR_UNSUPPORTED: D must be a multiple of 8 in [8, 16384]";
+        case ADALN_ERR_ALIGNMENT: return "ADALN_ERR_ALIGNMENT: misaligned pointer";
+        case ADALN_ERR_WORKSPACE: return "ADALN_ERR_WORKSPACE: workspace missing, too small or without status";
+        case ADALN_ERR_CUDA: return "ADALN_ERR_CUDA: CUDA runtime error";
+        case ADALN_ERR_BAD_SEQLENS: return "ADALN_ERR_BAD_SEQLENS: malformed cu_seqlens";
+        case ADALN_ERR_BAD_MOD_IDX: return "ADALN_ERR_BAD_MOD_IDX: mod_idx out of range";
+        default: return "unknown adaln status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,19 @@
+// Host-side entry points of the kernel translation units (internal to libadaln).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace adaln {
+
+cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, int tpb, int* out);
+cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, int64_t G, int tpb,
+                       cudaStream_t stream);
+
+cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, int tpb, int* out);
+cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, int64_t G, int tpb,
+                       cudaStream_t stream);
+cudaError_t launch_stage2(const Stage2Args& args, bool varlen, cudaStream_t stream);
+
+}  // namespace adaln

@@ -1,0 +1,481 @@
+#!/usr/bin/env python
+"""Benchmark of the fused AdaLN hot path on GB300.
+
+One step = one pass of the whole path over one batch: the dual-constraint bucket rule
+(host) that shapes the packed batch, the fused forward, the fused backward (dx plus
+per-tile D-tile partials) and the fixed-order reduction of dshift/dscale. The default
+workload is the packed mixed-length batch at D=3072, bf16 I/O (676 segments, 534,344
+tokens); its activations (3.3 GB per tensor) are far larger than L2, so no flush is
+needed between steps.
+
+Prints ONE JSON line (rank 0). `value` is algorithmic HBM bytes of forward + backward
+divided by the device time of a step (GB/s), summed over ranks; under torchrun every
+rank runs an independent replica (the path needs no collective to shard across
+replicas). `--impl reference` times the CPU oracle instead, on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "AdaLN fwd+bwd achieved HBM GB/s (% of GB300 peak) and Mtokens/s at D=3072"
+PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC = os.path.join(ROOT, "profiles", "bwd_partials_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+EPS = float(np.float32(1e-6))
+
+WORKLOADS = {
+    "packed": 3,          # the headline: packed mixed-length buckets, bf16, D=3072
+    "wan-1.3b": 1,
+    "wan-14b": 2,
+    "mmdit-f32": (4, synth.F32),
+    "mmdit-bf16": (4, synth.BF16),
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="packed")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------------------------------
+# workload and byte accounting
+# ------------------------------------------------------------------------------------------
+def make_workload(name: str, bucket_batch=None, generate=True) -> synth.Workload:
+    spec = WORKLOADS[name]
+    if spec == 3:
+        if bucket_batch is None:
+            import oracle
+            bucket_batch = oracle.bucket_batch
+        return synth.config(3, bucket_batch=bucket_batch, generate=generate)
+    if isinstance(spec, tuple):
+        return synth.config(spec[0], dtype=spec[1], generate=generate)
+    return synth.config(spec, generate=generate)
+
+
+def describe(w: synth.Workload) -> dict:
+    return {
+        "workload": w.name,
+        "tokens": w.R, "D": w.D, "segments": w.nseg, "modulation_rows": w.nmod,
+        "layout": "dense [Bt,N,D]" if w.dense else "packed cu_seqlens",
+        "io_dtype": synth.DTYPE_NAMES[w.dtype], "stats_and_grads": "f32",
+        "l2": "activations larger than L2 (%.2f GB per tensor); no flush" % (w.R * w.D * (2 if w.dtype == synth.BF16 else 4) / 1e9),
+        "parallelism": "replicas",
+    }
+
+
+def algorithmic_bytes(R: int, D: int, e: int, nmod: int) -> dict:
+    """Minimum HBM traffic of each call: every tensor it must read or write, once."""
+    fwd = R * D * e + R * D * e + 8 * R + 2 * nmod * D * e          # x, y, mean+rstd, shift+scale
+    partials = 2 * R * D * e + 8 * R + R * D * e + nmod * D * e      # dy, x, stats, dx, scale
+    reduce = 8 * nmod * D                                            # dshift, dscale
+    return {"fwd": fwd, "bwd_partials": partials, "bwd_reduce": reduce, "bwd": partials + reduce,
+            "step": fwd + partials + reduce}
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    for rel in ("adaln_layernorm_modulate_gb300/csrc/bwd.cu", "adaln_layernorm_modulate_gb300/csrc/common.cuh",
+                "adaln_layernorm_modulate_gb300/csrc/adaln.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the backward partials kernel from the committed ncu summary,
+    or None if it was taken on another workload or before the kernel last changed."""
+    try:
+        with open(TRAFFIC) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("workload") != workload or rec.get("source_sha256") != kernel_sources_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            import torch
+            ident = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            ident = str(device_index)
+        self.ident = ident
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for name, flag in zip(self.NAMES, parts[4:8]):
+                    if flag.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------------
+# distributed plumbing (replicas: barrier + max only)
+# ------------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ------------------------------------------------------------------------------------------
+def oracle_rows_time(orc, w: synth.Workload, r0: int, r1: int) -> float:
+    t0 = time.perf_counter()
+    _, mean, rstd = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod, eps=EPS,
+                            rows=(r0, r1))
+    orc.bwd(w.dy, w.x, mean.astype(np.float32), rstd.astype(np.float32), w.scale, w.dtype,
+            w.cu_seqlens, w.mod_idx, w.nmod, rows=(r0, r1))
+    return time.perf_counter() - t0
+
+
+def sample_bytes(w: synth.Workload, rows: int) -> int:
+    e = 2 if w.dtype == synth.BF16 else 4
+    b = algorithmic_bytes(rows, w.D, e, 0)
+    return b["fwd"] + b["bwd_partials"]
+
+
+def cpu_baseline(w: synth.Workload, seconds: float) -> dict:
+    import oracle
+    orc = oracle.get()
+    per_row = oracle_rows_time(orc, w, 0, 64) / 64
+    rows = int(min(w.R, max(64, seconds / max(per_row, 1e-9))))
+    dt = oracle_rows_time(orc, w, 0, rows)
+    gbs = sample_bytes(w, rows) / dt / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "forward + backward of the first %d of %d tokens (%.1f s, one thread, fp64)"
+                      % (rows, w.R, dt),
+            "mtokens_per_s": rows / dt / 1e6}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = make_workload(args.workload)
+    orc = oracle.get()
+    per_row = oracle_rows_time(orc, w, 0, 64) / 64
+    total_steps = args.steps + args.warmup
+    rows = int(max(16, min(w.R, 90.0 / total_steps / max(per_row, 1e-9))))
+    starts = np.random.default_rng(0).integers(0, max(1, w.R - rows), total_steps)
+    for i in range(args.warmup):
+        oracle_rows_time(orc, w, int(starts[i]), int(starts[i]) + rows)
+    t = 0.0
+    for i in range(args.warmup, total_steps):
+        t += oracle_rows_time(orc, w, int(starts[i]), int(starts[i]) + rows)
+    ms = t / args.steps * 1e3
+    gbs = sample_bytes(w, rows) / (ms / 1e3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(w),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step: forward + backward of %d consecutive tokens at a seeded "
+                                   "offset of the %d-token workload (one thread, fp64)" % (rows, w.R)},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "mtokens_per_s": rows / (ms / 1e3) / 1e6,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import adaln_layernorm_modulate_gb300 as A
+
+    world, rank, local = dist_env()
+    dist = dist_init(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    w = make_workload(args.workload, bucket_batch=A.adaln_bucket_batch)
+    e = 2 if w.dtype == synth.BF16 else 4
+    tdt = torch.bfloat16 if w.dtype == synth.BF16 else torch.float32
+    packed = w.dense is None
+
+    def host_tensor(a):
+        if w.dtype == synth.BF16 and a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(a)
+
+    h = {k: host_tensor(getattr(w, k)) for k in ("x", "dy", "shift", "scale")}
+    h["cu"] = torch.from_numpy(w.cu_seqlens.astype(np.int32))
+    h["mod"] = torch.from_numpy(w.mod_idx.astype(np.int32))
+    d = {k: v.to(dev) for k, v in h.items()}
+    R, D, nmod, nseg = w.R, w.D, w.nmod, w.nseg
+    y = torch.empty((R, D), dtype=tdt, device=dev)
+    dx = torch.empty((R, D), dtype=tdt, device=dev)
+    mean = torch.empty(R, dtype=torch.float32, device=dev)
+    rstd = torch.empty(R, dtype=torch.float32, device=dev)
+    dshift = torch.empty((nmod, D), dtype=torch.float32, device=dev)
+    dscale = torch.empty((nmod, D), dtype=torch.float32, device=dev)
+    if packed:
+        fws_n = A.adaln_fwd_varlen_workspace_size(R, nseg, D, w.dtype)
+        bws_n = A.adaln_bwd_varlen_workspace_size(R, nseg, nmod, D, w.dtype)
+    else:
+        fws_n = 0
+        bws_n = A.adaln_bwd_workspace_size(w.dense[0], w.dense[1], D, w.dtype)
+    fws = torch.empty(max(fws_n, 1), dtype=torch.uint8, device=dev)
+    bws = torch.empty(bws_n, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    buckets = w.meta.get("batches")
+
+    def shape_batch():
+        # Row a1 of the path: the bucket rule that sized this packed batch (host integers).
+        if buckets is not None:
+            got = [A.adaln_bucket_batch(S, synth.BUCKET_M_MEM, synth.BUCKET_M_COMP, synth.BUCKET_P)
+                   for S in synth.BUCKET_S]
+            if got != buckets:
+                raise RuntimeError("bucket sizes changed")
+
+    def fwd(x, shift, scale, cu, mod):
+        if packed:
+            A.adaln_fwd_varlen(x, shift, scale, y, mean, rstd, cu, mod, nseg, R, nmod, D, EPS, fws,
+                               fws_n, w.dtype, sptr)
+        else:
+            A.adaln_fwd(x, shift, scale, y, mean, rstd, w.dense[0], w.dense[1], D, EPS, w.dtype, sptr)
+
+    def bwd_stage(stage, dy, x, scale, cu, mod):
+        if packed:
+            fn = {"partials": A.adaln_bwd_varlen_partials, "reduce": A.adaln_bwd_varlen_reduce,
+                  "both": A.adaln_bwd_varlen}[stage]
+            fn(dy, x, mean, rstd, scale, dx, dshift, dscale, cu, mod, nseg, R, nmod, D, bws, bws_n,
+               w.dtype, sptr)
+        else:
+            fn = {"partials": A.adaln_bwd_partials, "reduce": A.adaln_bwd_reduce,
+                  "both": A.adaln_bwd}[stage]
+            fn(dy, x, mean, rstd, scale, dx, dshift, dscale, bws, bws_n, w.dense[0], w.dense[1], D,
+               w.dtype, sptr)
+
+    def step(ev):
+        shape_batch()
+        ev[0].record(stream)
+        fwd(d["x"], d["shift"], d["scale"], d["cu"], d["mod"])
+        ev[1].record(stream)
+        bwd_stage("partials", d["dy"], d["x"], d["scale"], d["cu"], d["mod"])
+        ev[2].record(stream)
+        bwd_stage("reduce", d["dy"], d["x"], d["scale"], d["cu"], d["mod"])
+        ev[3].record(stream)
+
+    def events(n):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+    for _ in range(args.warmup):
+        step(events(4))
+    if packed:
+        st = A.adaln_read_status(bws, sptr)
+        if st != 0:
+            raise RuntimeError("device status %s" % A.adaln_status_string(st))
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    step_events = [events(4) for _ in range(args.steps)]
+    t0, t1 = events(2)
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0.record(stream)
+    for ev in step_events:
+        step(ev)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clk = clocks.stop()
+
+    total_ms = t0.elapsed_time(t1)
+    ms_per_step = max_over_ranks(dist, total_ms / args.steps)
+    fwd_ms = float(np.mean([ev[0].elapsed_time(ev[1]) for ev in step_events]))
+    part_ms = float(np.mean([ev[1].elapsed_time(ev[2]) for ev in step_events]))
+    red_ms = float(np.mean([ev[2].elapsed_time(ev[3]) for ev in step_events]))
+
+    nb = algorithmic_bytes(R, D, e, nmod)
+    value = world * nb["step"] / (ms_per_step / 1e3) / 1e9
+    peak, peak_src = hbm_peak()
+
+    # End to end through the public calls, host buffers in and out, copies inside the region.
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        pin = {k: v.pin_memory() for k, v in h.items()}
+        out_h = {"y": torch.empty_like(y, device="cpu").pin_memory(),
+                 "dx": torch.empty_like(dx, device="cpu").pin_memory(),
+                 "mean": torch.empty_like(mean, device="cpu").pin_memory(),
+                 "rstd": torch.empty_like(rstd, device="cpu").pin_memory(),
+                 "dshift": torch.empty_like(dshift, device="cpu").pin_memory(),
+                 "dscale": torch.empty_like(dscale, device="cpu").pin_memory()}
+        outs = {"y": y, "dx": dx, "mean": mean, "rstd": rstd, "dshift": dshift, "dscale": dscale}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(v.numel() * v.element_size() for v in out_h.values())
+
+        def e2e_step():
+            for k, v in pin.items():
+                d[k].copy_(v, non_blocking=True)
+            shape_batch()
+            fwd(d["x"], d["shift"], d["scale"], d["cu"], d["mod"])
+            bwd_stage("both", d["dy"], d["x"], d["scale"], d["cu"], d["mod"])
+            for k, v in out_h.items():
+                v.copy_(outs[k], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = events(2)
+        barrier(dist)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        e2e_ms = max_over_ranks(dist, a.elapsed_time(b) / args.e2e_steps)
+        e2e = {"value": world * nb["step"] / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return 0
+    base = None if args.no_cpu_baseline else cpu_baseline(w, args.cpu_seconds)
+    achieved = nb["bwd_partials"] / (part_ms / 1e3) / 1e9
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": describe(w),
+        "pct_of_peak": 100.0 * value / (world * peak),
+        "mtokens_per_s": world * R / (ms_per_step / 1e3) / 1e6,
+        "per_call_us": {"fwd": fwd_ms * 1e3, "bwd_partials": part_ms * 1e3, "bwd_reduce": red_ms * 1e3,
+                        "bwd": (part_ms + red_ms) * 1e3},
+        "per_call_gbs": {"fwd": nb["fwd"] / fwd_ms / 1e6, "bwd": nb["bwd"] / (part_ms + red_ms) / 1e6},
+        "algorithmic_bytes_per_step": nb["step"],
+        "roofline": {"kernel": "bwd_kernel (fused dx + D-tile partials)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "peak_source": peak_src + " hbm_gbs",
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None if traffic is None else float(traffic),
+                     "algorithmic_bytes": nb["bwd_partials"]},
+        "cpu_baseline": base,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

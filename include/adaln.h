@@ -1,0 +1,169 @@
+/*
+ * libadaln — fused AdaLN (LayerNorm-Modulate) forward and backward for GB300 (sm_103a).
+ *
+ * The operator is the fused normalisation + modulation node of video / MMDiT diffusion
+ * transformers described in "AdaptiveLoad: Towards Efficient Video Diffusion Transformer
+ * Training" (technical summary, section 2.B "Fused LayerNorm-Modulate CUDA kernels").
+ * The pages name the operator without printing its formula; this library computes, for
+ * every token row x of width D that is modulated by row m of the shift/scale tables:
+ *
+ *     mean = (1/D) sum_d x_d,   var = (1/D) sum_d (x_d - mean)^2   (biased)
+ *     rstd = 1 / sqrt(var + eps),   xhat = (x - mean) * rstd       (no LayerNorm affine)
+ *     y    = xhat * (1 + scale[m]) + shift[m]
+ *
+ * and the gradients of a loss L with dL/dy = dy:
+ *
+ *     dx        = rstd * (g - mean_d(g) - xhat * mean_d(g * xhat)),  g = dy * (1 + scale[m])
+ *     dshift[m] = sum over tokens of m of dy,   dscale[m] = sum over tokens of m of dy * xhat
+ *
+ * The backward reduces dshift/dscale with threads pinned to a feature index d that
+ * accumulate down the sequence (the section's "D-tile coalesced reduction"), into per-tile
+ * fp32 partials that a second, fixed-order stage sums: results are bitwise reproducible
+ * run to run on the same device with the same arguments. No float atomics are used.
+ *
+ * Layouts (all row-major, D contiguous):
+ *   x, y, dy, dx      [R, D]   in `dtype`       R = Bt*N (dense) or total_tokens (packed)
+ *   shift, scale      [nmod, D] in `dtype`      dense: nmod = Bt, token (b, n) uses row b
+ *   mean, rstd        [R]      fp32
+ *   dshift, dscale    [nmod, D] fp32            (always fp32, also for bf16 I/O)
+ *   cu_seqlens        [nseg+1] int32 (device)   packed: cu_seqlens[0] = 0, non-decreasing,
+ *                                               cu_seqlens[nseg] = total_tokens
+ *   mod_idx           [nseg]   int32 (device)   segment s uses modulation row mod_idx[s]
+ *
+ * Ownership and execution. The caller owns every buffer. Every call is asynchronous and
+ * ordered on the caller's `stream`; nothing synchronises except adaln_read_status. The
+ * library allocates no device memory and keeps no state beyond cached device properties.
+ * Inputs and outputs must not alias.
+ *
+ * Preconditions (checked on the host; a violation returns a status and launches nothing):
+ *   - x, y, dy, dx, shift, scale, dshift, dscale: 16-byte aligned; mean, rstd: 4-byte
+ *     aligned; workspace: 256-byte aligned.
+ *   - 8 <= D <= 16384 and D % 8 == 0; eps > 0 and finite.
+ *   - Bt, N, total_tokens, nseg, nmod >= 0 (empty problems are valid: a backward with no
+ *     tokens writes zero gradients).
+ *
+ * Data errors in device-resident tables (cu_seqlens not starting at 0, decreasing, or not
+ * ending at total_tokens; mod_idx outside [0, nmod)) cannot be seen by the host. The
+ * kernels detect them, skip the affected rows without any out-of-range access, and record
+ * a code in the workspace; adaln_read_status returns it.
+ *
+ * Workspace. The packed forward and both backwards take a caller-allocated device
+ * workspace of at least the size the matching *_workspace_size function returns for the
+ * CURRENT device (the size depends on its SM count). It needs no initialisation.
+ * Determinism holds for a fixed device model: the tile split follows its SM count.
+ */
+#ifndef ADALN_H_
+#define ADALN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ADALN_F32 = 0, ADALN_BF16 = 1 } adaln_dtype;
+
+typedef enum {
+    ADALN_OK = 0,
+    ADALN_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad eps or dtype       */
+    ADALN_ERR_UNSUPPORTED = 2,  /* D outside [8, 16384] or not a multiple of 8          */
+    ADALN_ERR_ALIGNMENT = 3,    /* a pointer violates the alignment above               */
+    ADALN_ERR_WORKSPACE = 4,    /* workspace null or smaller than required              */
+    ADALN_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed          */
+    ADALN_ERR_BAD_SEQLENS = 6,  /* device data: cu_seqlens malformed (adaln_read_status) */
+    ADALN_ERR_BAD_MOD_IDX = 7   /* device data: mod_idx out of range (adaln_read_status) */
+} adaln_status;
+
+/* Forward, dense batch x[Bt, N, D]; token (b, n) uses shift[b], scale[b].
+ * Writes y, mean, rstd. Section 2.B, forward-pass bullet: statistics stay on chip, the
+ * row is reduced by warp shuffles then a block reduction, and the modulation is applied
+ * on a later pass over the row held in registers. One launch. */
+int adaln_fwd(const void* x, const void* shift, const void* scale, void* y, float* mean,
+              float* rstd, int64_t Bt, int64_t N, int64_t D, float eps, adaln_dtype dtype,
+              cudaStream_t stream);
+
+/* Workspace bytes adaln_bwd needs on the current device. */
+size_t adaln_bwd_workspace_size(int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype);
+
+/* Backward, dense batch. Reads dy, x, the forward's mean/rstd and scale; writes dx [Bt,N,D]
+ * and dshift/dscale [Bt, D] (fp32, overwritten). Section 2.B, backward-pass bullet ("D-tile
+ * coalesced reduction"): each row's dx is computed from the saved statistics while threads
+ * pinned to feature indices accumulate dy and dy*xhat down their tile of rows; per-tile
+ * partials are summed by a second, fixed-order stage. Two launches on `stream`. */
+int adaln_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+              const void* scale, void* dx, float* dshift, float* dscale, void* workspace,
+              size_t workspace_bytes, int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype,
+              cudaStream_t stream);
+
+/* The two stages of adaln_bwd as separate calls, taking adaln_bwd's exact arguments:
+ * adaln_bwd_partials launches only the fused dx + per-tile partial kernel (writes dx and the
+ * workspace partials; dshift/dscale untouched), adaln_bwd_reduce only the fixed-order
+ * second stage (reads the workspace partials, writes dshift/dscale). Calling both in this
+ * order on one stream is exactly adaln_bwd; they exist so each stage can be timed alone. */
+int adaln_bwd_partials(const void* dy, const void* x, const float* mean, const float* rstd,
+                       const void* scale, void* dx, float* dshift, float* dscale, void* workspace,
+                       size_t workspace_bytes, int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype,
+                       cudaStream_t stream);
+int adaln_bwd_reduce(const void* dy, const void* x, const float* mean, const float* rstd,
+                     const void* scale, void* dx, float* dshift, float* dscale, void* workspace,
+                     size_t workspace_bytes, int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype,
+                     cudaStream_t stream);
+
+/* Workspace bytes adaln_fwd_varlen needs (a small status area). */
+size_t adaln_fwd_varlen_workspace_size(int64_t total_tokens, int32_t nseg, int64_t D,
+                                       adaln_dtype dtype);
+
+/* Forward, packed mixed-length segments (x[total_tokens, D]); segment s uses modulation
+ * row mod_idx[s] of shift/scale [nmod, D]. Same math as adaln_fwd. */
+int adaln_fwd_varlen(const void* x, const void* shift, const void* scale, void* y, float* mean,
+                     float* rstd, const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                     int64_t total_tokens, int64_t nmod, int64_t D, float eps, void* workspace,
+                     size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream);
+
+/* Workspace bytes adaln_bwd_varlen needs on the current device. */
+size_t adaln_bwd_varlen_workspace_size(int64_t total_tokens, int32_t nseg, int64_t nmod,
+                                       int64_t D, adaln_dtype dtype);
+
+/* Backward, packed segments. dshift/dscale [nmod, D]: row m sums every token of every
+ * segment with mod_idx == m, in a fixed order; rows no segment uses are written as 0. */
+int adaln_bwd_varlen(const void* dy, const void* x, const float* mean, const float* rstd,
+                     const void* scale, void* dx, float* dshift, float* dscale,
+                     const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                     int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
+                     size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream);
+
+/* The two stages of adaln_bwd_varlen, with its exact arguments (see adaln_bwd_partials). */
+int adaln_bwd_varlen_partials(const void* dy, const void* x, const float* mean, const float* rstd,
+                              const void* scale, void* dx, float* dshift, float* dscale,
+                              const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                              int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
+                              size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream);
+int adaln_bwd_varlen_reduce(const void* dy, const void* x, const float* mean, const float* rstd,
+                            const void* scale, void* dx, float* dshift, float* dscale,
+                            const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
+                            int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
+                            size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns the device-side data status recorded in `workspace`
+ * by the last packed forward/backward (or backward) that used it: ADALN_OK,
+ * ADALN_ERR_BAD_SEQLENS or ADALN_ERR_BAD_MOD_IDX (ADALN_ERR_CUDA if the copy fails,
+ * ADALN_ERR_WORKSPACE if the workspace holds no status). */
+int adaln_read_status(const void* workspace, cudaStream_t stream);
+
+/* Dual-constraint bucket size, AdaptiveLoad technical summary section 2.A:
+ *     B = max(1, min(floor(M_mem / S), floor(M_comp / S^p)))
+ * with exact integer arithmetic (S^p is never formed past M_comp). Host only.
+ * Returns B >= 1, or -ADALN_ERR_INVALID_ARG when S, M_mem or M_comp <= 0 or p < 1. */
+int64_t adaln_bucket_batch(int64_t S, int64_t M_mem, int64_t M_comp, int32_t p);
+
+/* Static, human-readable name of a status code. */
+const char* adaln_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADALN_H_ */

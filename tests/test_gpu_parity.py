@@ -1,0 +1,316 @@
+"""CUDA path (through the C-ABI binding) against the CPU oracle on the same seeded bits.
+
+Small problems are compared element by element (several row tiles, ragged tails, odd
+segment tables, every row-width code path); the full-size workloads are compared on
+sampled rows and sampled modulation rows in the launch configuration the benchmark uses.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import synth
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import adaln_layernorm_modulate_gb300 as A
+    A.lib()  # loads the in-tree libadaln.so or raises
+
+
+def _oracle_full(orc, w, stats_rows=None):
+    y, mean, rstd = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod, eps=H.EPS)
+    return y, mean, rstd
+
+
+def _dx_terms(w, mean, rstd, rows):
+    """Oracle-side quantities for the statistics-shift bound of a pipeline comparison."""
+    x = synth.widen(w.x[rows[0]:rows[1]], w.dtype)
+    dy = synth.widen(w.dy[rows[0]:rows[1]], w.dtype)
+    m_of_row = np.repeat(w.mod_idx, np.diff(w.cu_seqlens))[rows[0]:rows[1]]
+    g = dy * (1 + synth.widen(w.scale, w.dtype)[m_of_row])
+    xhat = (x - mean[:, None]) * rstd[:, None]
+    return rstd, mean, xhat, g.mean(axis=1), (g * xhat).mean(axis=1)
+
+
+def _run_and_compare(orc, w):
+    d = H.upload(w)
+    y, mean, rstd, st = H.gpu_fwd(d)
+    assert st == 0
+    ry, rmean, rrstd = _oracle_full(orc, w)
+    H.check_io(H.to_host(y, w.dtype), ry, w.dtype, orc, "y")
+    H.check_stats(H.to_host(mean, 0), H.to_host(rstd, 0), rmean, rrstd)
+
+    # Isolated backward: both sides consume the oracle's statistics rounded to fp32.
+    m32, r32 = H.round_f32(rmean), H.round_f32(rrstd)
+    t = H.torch()
+    dm = t.from_numpy(m32.astype(np.float32)).cuda()
+    dr = t.from_numpy(r32.astype(np.float32)).cuda()
+    dx, dsh, dsc, st = H.gpu_bwd(d, dm, dr)
+    assert st == 0
+    rdx, rdsh, rdsc = orc.bwd(w.dy, w.x, m32, r32, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod)
+    H.check_io(H.to_host(dx, w.dtype), rdx, w.dtype, orc, "dx (isolated)")
+    assert H.rel_l2(H.to_host(dsh, 0), rdsh) <= H.grad_tol(w.dtype), "dshift (isolated)"
+    assert H.rel_l2(H.to_host(dsc, 0), rdsc) <= H.grad_tol(w.dtype), "dscale (isolated)"
+
+    # Pipeline backward: the GPU consumes its own forward statistics.
+    dx2, dsh2, dsc2, st = H.gpu_bwd(d, mean, rstd)
+    assert st == 0
+    extra = H.stat_shift_bound(_dx_terms(w, m32, r32, (0, w.R)))
+    H.check_io(H.to_host(dx2, w.dtype), rdx, w.dtype, orc, "dx (pipeline)", extra=extra)
+    assert H.rel_l2(H.to_host(dsh2, 0), rdsh) <= H.grad_tol(w.dtype), "dshift (pipeline)"
+    assert H.rel_l2(H.to_host(dsc2, 0), rdsc) <= H.grad_tol(w.dtype), "dscale (pipeline)"
+    # Rows of the modulation tables that no segment uses are exactly zero.
+    used = np.zeros(w.nmod, bool)
+    used[w.mod_idx[np.diff(w.cu_seqlens) > 0]] = True
+    assert np.all(H.to_host(dsh, 0)[~used] == 0) and np.all(H.to_host(dsc, 0)[~used] == 0)
+
+
+SMALL = {
+    "tiny-f32-2x256x128": lambda: synth.config(0),
+    "dense-bf16-2x300x1536": lambda: synth.dense("c", 101, synth.BF16, 2, 300, 1536,
+                                                 x_mode=synth.ROWS_SCALED, dy_std=0.02),
+    "dense-bf16-1x333x5120": lambda: synth.dense("c", 102, synth.BF16, 1, 333, 5120,
+                                                 x_mode=synth.ROWS_SCALED, dy_std=0.02),
+    "dense-f32-2x129x3072": lambda: synth.dense("c", 103, synth.F32, 2, 129, 3072,
+                                                x_mode=synth.ROWS_SCALED, dy_std=0.02),
+    "packed-bf16-d3072-ragged": lambda: synth.make("c", 104, synth.BF16, 3072,
+                                                   [1, 7, 256, 1000, 3, 0, 513],
+                                                   [4, 0, 2, 2, 5, 1, 0], 6,
+                                                   x_mode=synth.ROWS_SCALED, dy_std=0.02),
+    "packed-f32-d3072-adversarial": lambda: synth.make("c", 105, synth.F32, 3072, [40, 300, 17, 129],
+                                                       [0, 2, 1, 3], 4, x_mode=synth.ROWS_ADVERSARIAL,
+                                                       mod_std=0.5, dy_std=0.02),
+    "packed-bf16-d3072-adversarial": lambda: synth.make("c", 106, synth.BF16, 3072, [40, 300, 17, 129],
+                                                        [0, 2, 1, 3], 4, x_mode=synth.ROWS_ADVERSARIAL,
+                                                        mod_std=0.5, dy_std=0.02),
+    "dense-bf16-d8": lambda: synth.dense("c", 107, synth.BF16, 3, 50, 8),
+    "packed-bf16-d264": lambda: synth.make("c", 108, synth.BF16, 264, [5, 90, 33], [1, 1, 0], 2),
+    "dense-bf16-d16384": lambda: synth.dense("c", 109, synth.BF16, 1, 40, 16384, dy_std=0.1),
+    "dense-f32-d8192": lambda: synth.dense("c", 110, synth.F32, 1, 33, 8192),
+    "packed-f32-d128-many": lambda: synth.make(
+        "c", 111, synth.F32, 128, list(np.random.default_rng(5).integers(0, 10, 100)),
+        list(np.random.default_rng(6).integers(0, 13, 100)), 13),
+    "dense-f32-one-row": lambda: synth.dense("c", 112, synth.F32, 1, 1, 1536),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_elementwise(orc, name):
+    _run_and_compare(orc, SMALL[name]())
+
+
+def _oracle_rows(orc, w, r0, r1):
+    y, mean, rstd = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod,
+                            eps=H.EPS, rows=(r0, r1))
+    m32, r32 = H.round_f32(mean), H.round_f32(rstd)
+    dx, _, _ = orc.bwd(w.dy, w.x, m32, r32, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod,
+                       rows=(r0, r1))
+    return y, mean, rstd, dx, m32, r32
+
+
+def _sample_blocks(w, rng, per_segment=2, random_rows=48):
+    blocks = []
+    for s in range(w.nseg):
+        a, b = int(w.cu_seqlens[s]), int(w.cu_seqlens[s + 1])
+        if b > a:
+            blocks.append((a, min(b, a + per_segment)))
+            blocks.append((max(a, b - per_segment), b))
+    for r in rng.integers(0, w.R, random_rows):
+        blocks.append((int(r), int(r) + 1))
+    return sorted(set(blocks))
+
+
+def _full_size(orc, w, sample_mods):
+    t = H.torch()
+    d = H.upload(w)
+    y, mean, rstd, st = H.gpu_fwd(d)
+    assert st == 0
+    dx, dsh, dsc, st = H.gpu_bwd(d, mean, rstd)
+    assert st == 0
+    rng = np.random.default_rng(w.seed + 1000)
+    for r0, r1 in _sample_blocks(w, rng):
+        ry, rmean, rrstd, rdx, m32, r32 = _oracle_rows(orc, w, r0, r1)
+        H.check_io(H.to_host(y[r0:r1], w.dtype), ry, w.dtype, orc, "y rows %d:%d" % (r0, r1))
+        H.check_stats(H.to_host(mean[r0:r1], 0), H.to_host(rstd[r0:r1], 0), rmean, rrstd)
+        extra = H.stat_shift_bound(_dx_terms(w, m32, r32, (r0, r1)))
+        H.check_io(H.to_host(dx[r0:r1], w.dtype), rdx, w.dtype, orc, "dx rows %d:%d" % (r0, r1),
+                   extra=extra)
+    dsh_h, dsc_h = H.to_host(dsh, 0), H.to_host(dsc, 0)
+    for m in sample_mods:
+        ref_sh = np.zeros((w.nmod, w.D))
+        ref_sc = np.zeros((w.nmod, w.D))
+        for s in np.nonzero(w.mod_idx == m)[0]:
+            a, b = int(w.cu_seqlens[s]), int(w.cu_seqlens[s + 1])
+            for c0 in range(a, b, 8192):
+                c1 = min(b, c0 + 8192)
+                _, mu, rs = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod,
+                                    eps=H.EPS, rows=(c0, c1))
+                orc.bwd(w.dy, w.x, H.round_f32(mu), H.round_f32(rs), w.scale, w.dtype, w.cu_seqlens,
+                        w.mod_idx, w.nmod, rows=(c0, c1), dshift=ref_sh, dscale=ref_sc)
+        assert H.rel_l2(dsh_h[m], ref_sh[m]) <= H.grad_tol(w.dtype), "dshift[%d]" % m
+        assert H.rel_l2(dsc_h[m], ref_sc[m]) <= H.grad_tol(w.dtype), "dscale[%d]" % m
+    del d, y, dx
+    t.cuda.empty_cache()
+
+
+def test_full_wan_1_3b(orc):
+    _full_size(orc, synth.config(1), [0])
+
+
+def test_full_wan_14b(orc):
+    _full_size(orc, synth.config(2), [0])
+
+
+def test_full_packed_buckets(orc):
+    import adaln_layernorm_modulate_gb300 as A
+    w = synth.config(3, bucket_batch=A.adaln_bucket_batch)
+    assert w.meta["batches"] == [512, 128, 32, 2, 1, 1]
+    _full_size(orc, w, [0, 511, 512, 639, 640, 671, 673, 674, 675])
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16], ids=["f32", "bf16"])
+def test_full_mmdit(orc, dtype):
+    _full_size(orc, synth.config(4, dtype=dtype), [0, 1, 2, 3])
+
+
+def test_backward_is_bitwise_deterministic():
+    for w in (synth.dense("det", 201, synth.BF16, 1, 4000, 1536, x_mode=synth.ROWS_SCALED, dy_std=0.02),
+              synth.make("det", 202, synth.BF16, 3072, [300, 5, 2000, 77], [1, 0, 1, 2], 3,
+                         x_mode=synth.ROWS_SCALED, dy_std=0.02)):
+        d = H.upload(w)
+        y, mean, rstd, _ = H.gpu_fwd(d)
+        ref = [H.to_host(v, w.dtype if i == 0 else 0) for i, v in enumerate(H.gpu_bwd(d, mean, rstd)[:3])]
+        for _ in range(4):
+            y2, mean2, rstd2, _ = H.gpu_fwd(d)
+            assert H.torch().equal(y, y2) and H.torch().equal(mean, mean2)
+            got = [H.to_host(v, w.dtype if i == 0 else 0) for i, v in enumerate(H.gpu_bwd(d, mean, rstd)[:3])]
+            for a, b in zip(ref, got):
+                assert np.array_equal(a, b)
+
+
+def test_packed_equals_dense_streams():
+    """The MMDiT packed call (4 segments) gives bitwise the per-row results of the dense
+    per-stream calls: row math does not depend on which tile holds the row."""
+    t = H.torch()
+    T, V, D = 64, 700, 3072
+    w = synth.make("mm", 301, synth.BF16, D, [T, V, T, V], [0, 2, 1, 3], 4,
+                   x_mode=synth.ROWS_ADVERSARIAL, mod_std=0.5, dy_std=0.02)
+    d = H.upload(w)
+    y, mean, rstd, st = H.gpu_fwd(d)
+    dx, dsh, dsc, _ = H.gpu_bwd(d, mean, rstd)
+    assert st == 0
+    cu = w.cu_seqlens
+    for rows_of, table_rows, N in (([0, 2], [0, 1], T), ([1, 3], [2, 3], V)):
+        xs = np.concatenate([w.x[cu[s]:cu[s + 1]] for s in rows_of])
+        dys = np.concatenate([w.dy[cu[s]:cu[s + 1]] for s in rows_of])
+        ws = synth.Workload("stream", 0, w.dtype, D, np.array([0, N, 2 * N]), np.array([0, 1]), 2,
+                            dense=(2, N), x=xs, dy=dys, shift=w.shift[table_rows], scale=w.scale[table_rows])
+        dd = H.upload(ws)
+        y2, mean2, rstd2, _ = H.gpu_fwd(dd)
+        dx2, dsh2, dsc2, _ = H.gpu_bwd(dd, mean2, rstd2)
+        idx = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in rows_of])
+        it = t.from_numpy(idx).cuda()
+        assert t.equal(y[it], y2) and t.equal(mean[it], mean2) and t.equal(rstd[it], rstd2)
+        assert t.equal(dx[it], dx2)
+        np.testing.assert_allclose(H.to_host(dsh[table_rows], 0), H.to_host(dsh2, 0), rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(H.to_host(dsc[table_rows], 0), H.to_host(dsc2, 0), rtol=1e-5, atol=1e-5)
+
+
+def test_malformed_tables_report_status_without_faulting():
+    import adaln_layernorm_modulate_gb300 as A
+    t = H.torch()
+    w = synth.make("bad", 401, synth.BF16, 256, [10, 20, 30], [0, 1, 2], 3)
+    d = H.upload(w)
+    good_cu, good_mod = d.cu.clone(), d.mod.clone()
+    cases = [
+        ("decreasing", lambda: d.cu.copy_(t.tensor([0, 25, 5, 60], dtype=t.int32)), A.STATUS[6]),
+        ("short total", lambda: d.cu.copy_(t.tensor([0, 10, 30, 50], dtype=t.int32)), A.STATUS[6]),
+        ("nonzero start", lambda: d.cu.copy_(t.tensor([3, 10, 30, 60], dtype=t.int32)), A.STATUS[6]),
+        ("beyond total", lambda: d.cu.copy_(t.tensor([0, 10, 90, 60], dtype=t.int32)), A.STATUS[6]),
+        ("mod too large", lambda: d.mod.copy_(t.tensor([0, 3, 2], dtype=t.int32)), A.STATUS[7]),
+        ("mod negative", lambda: d.mod.copy_(t.tensor([-1, 1, 2], dtype=t.int32)), A.STATUS[7]),
+    ]
+    for name, corrupt, want in cases:
+        d.cu.copy_(good_cu)
+        d.mod.copy_(good_mod)
+        corrupt()
+        _, mean, rstd, st = H.gpu_fwd(d)
+        assert A.STATUS[st] == want, (name, A.STATUS[st])
+        _, _, _, st = H.gpu_bwd(d, mean, rstd)
+        assert A.STATUS[st] == want, (name, A.STATUS[st])
+        t.cuda.synchronize()
+    d.cu.copy_(good_cu)
+    d.mod.copy_(good_mod)
+    _, mean, rstd, st = H.gpu_fwd(d)
+    assert st == 0
+    assert H.gpu_bwd(d, mean, rstd)[3] == 0
+
+
+def test_empty_and_zero_length_segments(orc):
+    import adaln_layernorm_modulate_gb300 as A
+    t = H.torch()
+    # Dense backward over no tokens: zero gradients.
+    D = 512
+    dsh = t.full((3, D), 7.0, device="cuda")
+    dsc = t.full((3, D), 7.0, device="cuda")
+    nb = A.adaln_bwd_workspace_size(3, 0, D, A.ADALN_BF16)
+    ws = t.empty(nb, dtype=t.uint8, device="cuda")
+    A.adaln_bwd(None, None, None, None, None, None, dsh, dsc, ws, nb, 3, 0, D, A.ADALN_BF16)
+    assert t.count_nonzero(dsh) == 0 and t.count_nonzero(dsc) == 0
+    # Packed tables whose segments are all empty.
+    w = synth.make("empty", 501, synth.F32, D, [0, 0, 0], [0, 1, 1], 2)
+    d = H.upload(w)
+    _, mean, rstd, st = H.gpu_fwd(d)
+    assert st == 0
+    _, dsh, dsc, st = H.gpu_bwd(d, mean, rstd)
+    assert st == 0 and t.count_nonzero(dsh) == 0 and t.count_nonzero(dsc) == 0
+    # Empty segments between non-empty ones, leading and trailing.
+    _run_and_compare(orc, synth.make("gaps", 502, synth.F32, D, [0, 3, 0, 0, 5, 0], [0, 1, 2, 0, 1, 2], 3))
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Guard bands around every output keep their fill pattern."""
+    import adaln_layernorm_modulate_gb300 as A
+    t = H.torch()
+    w = synth.make("guard", 601, synth.BF16, 1536, [3, 130, 1, 66], [2, 0, 1, 1], 3,
+                   x_mode=synth.ROWS_SCALED, dy_std=0.02)
+    d = H.upload(w)
+    G = 4096  # guard elements on each side (multiple of 8 keeps 16-byte alignment)
+
+    def guarded(n, dtype):
+        buf = t.empty(n + 2 * G, dtype=dtype, device="cuda")
+        buf.view(t.uint8).fill_(0xA5) if dtype != t.float32 else buf.view(t.int32).fill_(0x5A5A5A5A)
+        return buf, buf[G:G + n]
+
+    def intact(buf, n):
+        raw = buf.view(t.uint8) if buf.dtype != t.float32 else buf.view(t.int32)
+        k = raw.numel() // buf.numel()
+        head, tail = raw[:G * k], raw[(G + n) * k:]
+        want = 0xA5 if buf.dtype != t.float32 else 0x5A5A5A5A
+        return bool((head == want).all()) and bool((tail == want).all())
+
+    yb, y = guarded(w.R * w.D, t.bfloat16)
+    mb, mean = guarded(w.R, t.float32)
+    rb, rstd = guarded(w.R, t.float32)
+    nb = A.adaln_fwd_varlen_workspace_size(w.R, w.nseg, w.D, w.dtype)
+    ws = t.empty(nb, dtype=t.uint8, device="cuda")
+    A.adaln_fwd_varlen(d.x, d.shift, d.scale, y, mean, rstd, d.cu, d.mod, w.nseg, w.R, w.nmod, w.D,
+                       H.EPS, ws, nb, w.dtype)
+    dxb, dx = guarded(w.R * w.D, t.bfloat16)
+    shb, dsh = guarded(w.nmod * w.D, t.float32)
+    scb, dsc = guarded(w.nmod * w.D, t.float32)
+    nb = A.adaln_bwd_varlen_workspace_size(w.R, w.nseg, w.nmod, w.D, w.dtype)
+    ws2 = t.empty(nb, dtype=t.uint8, device="cuda")
+    A.adaln_bwd_varlen(d.dy, d.x, mean, rstd, d.scale, dx, dsh, dsc, d.cu, d.mod, w.nseg, w.R, w.nmod,
+                       w.D, ws2, nb, w.dtype)
+    t.cuda.synchronize()
+    for buf, n in ((yb, w.R * w.D), (mb, w.R), (rb, w.R), (dxb, w.R * w.D), (shb, w.nmod * w.D),
+                   (scb, w.nmod * w.D)):
+        assert intact(buf, n)
