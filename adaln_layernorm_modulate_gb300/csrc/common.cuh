@@ -145,9 +145,12 @@ __device__ uint32_t validate_segments(const Segments& sg, int64_t b, int64_t G) 
 
 // Every CTA stores its status word (no zeroing, no atomics); CTA 0 stamps the header.
 __device__ __forceinline__ void publish_status(uint32_t err, uint32_t* words, WsHeader* header) {
-    err = (uint32_t)__syncthreads_or((int)err);
+    // __syncthreads_or answers only "any thread non-zero?", so combine bit by bit.
+    uint32_t all = 0;
+    if (__syncthreads_or((int)(err & kErrSeqlens))) all |= kErrSeqlens;
+    if (__syncthreads_or((int)(err & kErrModIdx))) all |= kErrModIdx;
     if (words == nullptr || threadIdx.x != 0) return;
-    words[blockIdx.x] = err;
+    words[blockIdx.x] = all;
     if (blockIdx.x == 0) {
         header->magic = kStatusMagic;
         header->nwords = gridDim.x;
