@@ -30,8 +30,9 @@ EXPORTS = (
     "adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd", "adaln_bwd_partials", "adaln_bwd_reduce",
     "adaln_fwd_varlen_workspace_size", "adaln_fwd_varlen", "adaln_bwd_varlen_workspace_size",
     "adaln_bwd_varlen", "adaln_bwd_varlen_partials", "adaln_bwd_varlen_reduce",
-    "adaln_read_status", "adaln_bucket_batch", "adaln_status_string",
+    "adaln_read_status", "adaln_bwd_noalloc", "adaln_bucket_batch", "adaln_status_string",
 )
+NOALLOC_SCRATCH_BYTES = 16 << 20  # ADALN_NOALLOC_SCRATCH_BYTES
 
 
 class AdalnError(RuntimeError):
@@ -65,6 +66,7 @@ def _load() -> ctypes.CDLL:
         "adaln_bwd_varlen_reduce": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64,
                                      vp, sz, ci, vp], ci),
         "adaln_read_status": ([vp, vp], ci),
+        "adaln_bwd_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp], ci),
         "adaln_bucket_batch": ([i64, i64, i64, i32], i64),
         "adaln_status_string": ([ci], ctypes.c_char_p),
     }
@@ -201,6 +203,15 @@ def adaln_bwd_varlen_reduce(dy, x, mean, rstd, scale, dx, dshift, dscale, cu_seq
 
 def adaln_read_status(workspace, stream=None) -> int:
     return int(lib().adaln_read_status(_ptr(workspace), _stream(stream)))
+
+
+def adaln_bwd_noalloc(dy, x, mean, rstd, scale, dx, dshift, dscale, Bt, N, D, dtype=None,
+                      stream=None):
+    """adaln_bwd without a workspace, for callers that cannot allocate device memory; its
+    scratch is a fixed array inside the library (see include/adaln.h)."""
+    _check("adaln_bwd_noalloc", lib().adaln_bwd_noalloc(
+        _ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale), _ptr(dx), _ptr(dshift),
+        _ptr(dscale), Bt, N, D, _dtype(dtype, dy), _stream(stream)))
 
 
 def adaln_bucket_batch(S, M_mem, M_comp, p) -> int:

@@ -419,3 +419,55 @@ const char* adaln_status_string(int status) {
 }
 
 }  // extern "C"
+
+// ---- dense backward without a caller workspace ---------------------------------------------
+//
+// Some callers cannot allocate device memory at the point where they run the backward: a
+// host framework that hands out only the tensors it owns, code running under an allocator
+// that must not grow, or a plain C caller with no allocator at all. For them the backward's
+// scratch (status words and per-tile partials) lives in one fixed array that is part of
+// this module: every GPU that loads the library holds ADALN_NOALLOC_SCRATCH_BYTES of it
+// until the process exits.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ADALN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// The array's device address on the current device. In host code the array's name only
+// stands in for the symbol, so the address must come from the runtime, once per device,
+// with that device current.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ADALN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return ADALN_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return ADALN_OK;
+}
+
+}  // namespace
+
+extern "C" int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean,
+                                 const float* rstd, const void* scale, void* dx, float* dshift,
+                                 float* dscale, int64_t Bt, int64_t N, int64_t D,
+                                 adaln_dtype dtype, cudaStream_t stream) {
+    // The scratch needs no clearing: every call writes each status word and each partial it
+    // later reads.
+    if (int rc = check_shape(D, dtype)) return rc;
+    if (Bt < 0 || N < 0) return ADALN_ERR_INVALID_ARG;
+    if (Bt == 0) return ADALN_OK;
+    void* scratch = nullptr;
+    if (int rc = noalloc_scratch(&scratch)) return rc;
+    // bwd_dense returns ADALN_ERR_WORKSPACE, before launching anything, when the problem
+    // needs more scratch than the fixed array holds.
+    return bwd_dense(dy, x, mean, rstd, scale, dx, dshift, dscale, scratch,
+                     (size_t)ADALN_NOALLOC_SCRATCH_BYTES, Bt, N, D, dtype, stream, kBoth);
+}

@@ -32,7 +32,8 @@
  *
  * Ownership and execution. The caller owns every buffer. Every call is asynchronous and
  * ordered on the caller's `stream`; nothing synchronises except adaln_read_status. The
- * library allocates no device memory and keeps no state beyond cached device properties.
+ * library allocates no device memory and keeps no state beyond cached device properties
+ * (adaln_bwd_noalloc's fixed scratch array, below, is part of the loaded module).
  * Inputs and outputs must not alias.
  *
  * Preconditions (checked on the host; a violation returns a status and launches nothing):
@@ -152,6 +153,30 @@ int adaln_bwd_varlen_reduce(const void* dy, const void* x, const float* mean, co
  * ADALN_ERR_BAD_SEQLENS or ADALN_ERR_BAD_MOD_IDX (ADALN_ERR_CUDA if the copy fails,
  * ADALN_ERR_WORKSPACE if the workspace holds no status). */
 int adaln_read_status(const void* workspace, cudaStream_t stream);
+
+/* Bytes of the fixed scratch array adaln_bwd_noalloc uses on every device that loads the
+ * library (16 MiB). */
+#define ADALN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* adaln_bwd for callers that cannot allocate device memory (no caller workspace).
+ * The paper has no counterpart to this call; it exists for callers such as a host framework
+ * that only hands out the tensors it owns, code that runs under an allocator that must not
+ * grow, or a plain C program without a device allocator. Same arguments and results as
+ * adaln_bwd minus the workspace: the scratch is a fixed array of ADALN_NOALLOC_SCRATCH_BYTES
+ * inside this library, held by every GPU that loads the library until the process exits.
+ *   - Allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - Problems whose scratch need, adaln_bwd_workspace_size(Bt, N, D, dtype), exceeds
+ *     ADALN_NOALLOC_SCRATCH_BYTES are rejected with ADALN_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's contents;
+ *     nothing in it needs to start at zero. Calls that overlap on the GPU (different
+ *     streams, or different host threads, without ordering between them) race on it and
+ *     give wrong gradients: order them on one stream. */
+int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean, const float* rstd,
+                      const void* scale, void* dx, float* dshift, float* dscale, int64_t Bt,
+                      int64_t N, int64_t D, adaln_dtype dtype, cudaStream_t stream);
 
 /* Dual-constraint bucket size, AdaptiveLoad technical summary section 2.A:
  *     B = max(1, min(floor(M_mem / S), floor(M_comp / S^p)))
