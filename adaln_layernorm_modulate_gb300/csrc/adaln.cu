@@ -35,32 +35,78 @@ int current_sms(int* dev_out) {
 }
 
 // How a row of width D is spread over a CTA: each thread owns `nv` 16-byte vectors
-// (v = tid + k * tpb), so a CTA holds one row in registers.
+// (v = tid + k * tpb), so a CTA holds one row in registers. The per-row reduction work is
+// paid once per thread per row, so more elements per thread amortise it better, until
+// registers run out: the forward holds about 32 elements a thread, the backward (which
+// keeps twice as many values per element) about 16. Narrow rows shrink nv so a warp is not
+// left idle; wide rows grow it so a row fits the CTA size the kernel is compiled for
+// (RowShape<nv>::kMaxThreads).
 struct RowCfg {
     int nv;
     int tpb;
+    bool full;  // nv * tpb vectors == the row: no idle lanes
 };
 
-RowCfg row_cfg(int64_t D, adaln_dtype dtype) {
+int max_threads_for(int nv) { return nv == 1 || nv >= 8 ? 512 : 384; }
+
+RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
+    static const int kNv[] = {1, 2, 4, 8};
     const int64_t VE = dtype == ADALN_BF16 ? 8 : 4;
     const int64_t V = D / VE;
-    int64_t nv = (V + 511) / 512;
-    if (nv < 1) nv = 1;
-    if (nv > 4) nv = 4;
-    const int64_t per = (V + nv - 1) / nv;
-    return RowCfg{(int)nv, (int)((per + 31) / 32 * 32)};
+    int64_t target = (forward ? 32 : 16) / VE;
+    if ((V + 31) / 32 < target) target = (V + 31) / 32;
+    if (target < 1) target = 1;
+    for (int nv : kNv) {
+        if (nv < target) continue;
+        const int64_t tpb = ((V + nv - 1) / nv + 31) / 32 * 32;
+        if (tpb <= max_threads_for(nv)) return RowCfg{nv, (int)tpb, V == nv * tpb};
+    }
+    const int64_t tpb = ((V + 7) / 8 + 31) / 32 * 32;
+    return RowCfg{8, (int)tpb, V == 8 * tpb};
 }
 
 enum Kind { kFwd = 0, kBwd = 1 };
 
-// Row tiles of one launch: every resident CTA slot of the device, at most one per row.
-int64_t plan_tiles(Kind kind, adaln_dtype dtype, const RowCfg& c, bool varlen, int64_t R,
-                   int* sms_out) {
+// Shared memory a CTA may give its cp.async ring: two such CTAs fit on one SM.
+constexpr size_t kRingBudget = 100 * 1024;
+
+struct Plan {
+    RowCfg c;
+    bool ring;      // cp.async shared-memory ring (false: plain loads into registers)
+    bool full;      // ring kernel specialised for rows the CTA covers exactly
+    int stages;     // ring depth in rounds
+    size_t smem;    // dynamic shared memory per CTA
+    int64_t G;      // row tiles = CTAs
+    int sms;
+};
+
+// One ring round: RB rows of this CTA's vectors of x (and dy for the backward), plus one
+// 4-byte word per thread and per-row scalar (K in the forward, mean and rstd backward).
+size_t ring_round_bytes(Kind kind, const RowCfg& c) {
+    const size_t rb = c.nv <= 2 ? 2 : 1;  // RowShape<nv>::kRows
+    const size_t row = (size_t)c.tpb * c.nv * 16;
+    const size_t words = (size_t)c.tpb * 4;
+    return kind == kFwd ? rb * (row + words) : rb * (2 * row + 2 * words);
+}
+
+// Launch plan: ring depth from the budget, and row tiles = every resident CTA slot of the
+// device (at most one per row).
+bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, Plan* p) {
     int dev = 0;
     const int sms = current_sms(&dev);
-    if (sms <= 0) return -1;
-    *sms_out = sms;
-    const auto key = std::make_tuple(dev, (int)kind, (int)dtype, c.nv, (int)varlen, c.tpb);
+    if (sms <= 0) return false;
+    p->sms = sms;
+    p->c = row_cfg(D, dtype, kind == kFwd);
+    const size_t round = ring_round_bytes(kind, p->c);
+    size_t stages = kRingBudget / round;
+    if (stages > (size_t)kMaxStages) stages = kMaxStages;
+    p->ring = stages >= 2;
+    p->full = p->ring && p->c.full;
+    p->stages = p->ring ? (int)stages : 0;
+    p->smem = p->ring ? stages * round : 0;
+    const auto key = std::make_tuple(dev, (int)kind, (int)dtype, p->c.nv,
+                                     (int)varlen * 4 + (int)p->ring * 2 + (int)p->full,
+                                     p->c.tpb * 16 + p->stages);
     int bps = 0;
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -68,9 +114,11 @@ int64_t plan_tiles(Kind kind, adaln_dtype dtype, const RowCfg& c, bool varlen, i
         if (it != g_occupancy.end()) bps = it->second;
     }
     if (bps == 0) {
-        const cudaError_t e = kind == kFwd ? fwd_blocks_per_sm((int)dtype, c.nv, varlen, c.tpb, &bps)
-                                           : bwd_blocks_per_sm((int)dtype, c.nv, varlen, c.tpb, &bps);
-        if (e != cudaSuccess || bps <= 0) return -1;
+        const cudaError_t e =
+            kind == kFwd
+                ? fwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring, p->full, p->c.tpb, p->smem, &bps)
+                : bwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring, p->full, p->c.tpb, p->smem, &bps);
+        if (e != cudaSuccess || bps <= 0) return false;
         std::lock_guard<std::mutex> lock(g_mu);
         g_occupancy[key] = bps;
     }
@@ -78,7 +126,8 @@ int64_t plan_tiles(Kind kind, adaln_dtype dtype, const RowCfg& c, bool varlen, i
     if (G > kMaxCtas) G = kMaxCtas;
     if (G > R) G = R;
     if (G < 1) G = 1;
-    return G;
+    p->G = G;
+    return true;
 }
 
 // float4 columns per stage-2 CTA: aim for ~4 CTAs per SM over all modulation rows.
@@ -142,10 +191,8 @@ Segments packed_segments(const int32_t* cu, const int32_t* mod, int32_t nseg, in
 int run_fwd(const void* x, const void* shift, const void* scale, void* y, float* mean,
             float* rstd, const Segments& seg, int64_t D, float eps, void* ws, bool varlen,
             adaln_dtype dtype, cudaStream_t stream) {
-    const RowCfg c = row_cfg(D, dtype);
-    int sms = 0;
-    const int64_t G = plan_tiles(kFwd, dtype, c, varlen, seg.R, &sms);
-    if (G < 0) return ADALN_ERR_CUDA;
+    Plan p;
+    if (!make_plan(kFwd, dtype, D, varlen, seg.R, &p)) return ADALN_ERR_CUDA;
     FwdArgs a{};
     a.x = x;
     a.shift = shift;
@@ -158,11 +205,15 @@ int run_fwd(const void* x, const void* shift, const void* scale, void* y, float*
     a.seg = seg;
     a.status = ws ? reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kHeaderBytes) : nullptr;
     a.header = static_cast<WsHeader*>(ws);
-    return launched(launch_fwd(a, (int)dtype, c.nv, varlen, G, c.tpb, stream));
+    a.stages = p.stages;
+    return launched(
+        launch_fwd(a, (int)dtype, p.c.nv, varlen, p.ring, p.full, p.G, p.c.tpb, p.smem, stream));
 }
 
-int64_t bwd_tiles(int64_t R, int64_t D, bool varlen, adaln_dtype dtype, int* sms) {
-    return plan_tiles(kBwd, dtype, row_cfg(D, dtype), varlen, R, sms);
+int64_t bwd_tiles(int64_t R, int64_t D, bool varlen, adaln_dtype dtype) {
+    Plan p;
+    if (!make_plan(kBwd, dtype, D, varlen, R, &p)) return -1;
+    return p.G;
 }
 
 enum Stages { kPartials = 1, kReduce = 2, kBoth = 3 };
@@ -172,10 +223,9 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
             int64_t D, void* ws, size_t ws_bytes, bool varlen, adaln_dtype dtype,
             cudaStream_t stream, int stages) {
     if (int rc = check_workspace(ws, ws_bytes, kPartialsOffset)) return rc;
-    const RowCfg c = row_cfg(D, dtype);
-    int sms = 0;
-    const int64_t G = plan_tiles(kBwd, dtype, c, varlen, seg.R, &sms);
-    if (G < 0) return ADALN_ERR_CUDA;
+    Plan p;
+    if (!make_plan(kBwd, dtype, D, varlen, seg.R, &p)) return ADALN_ERR_CUDA;
+    const int64_t G = p.G;
     if (int rc = check_workspace(ws, ws_bytes, bwd_need(G, seg.nseg, D))) return rc;
     char* base = static_cast<char*>(ws);
     BwdArgs a{};
@@ -190,8 +240,11 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
     a.seg = seg;
     a.status = reinterpret_cast<uint32_t*>(base + kHeaderBytes);
     a.header = reinterpret_cast<WsHeader*>(base);
+    a.stages = p.stages;
     if (stages & kPartials) {
-        if (int rc = launched(launch_bwd(a, (int)dtype, c.nv, varlen, G, c.tpb, stream))) return rc;
+        if (int rc = launched(launch_bwd(a, (int)dtype, p.c.nv, varlen, p.ring, p.full, G, p.c.tpb,
+                                         p.smem, stream)))
+            return rc;
     }
     if (!(stages & kReduce) || seg.nmod == 0) return ADALN_OK;
     Stage2Args s{};
@@ -200,7 +253,7 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
     s.dscale = dscale;
     s.D = D;
     s.G = G;
-    s.cw = stage2_cw(D, seg.nmod, sms);
+    s.cw = stage2_cw(D, seg.nmod, p.sms);
     s.seg = seg;
     return launched(launch_stage2(s, varlen, stream));
 }
@@ -226,8 +279,7 @@ int adaln_fwd(const void* x, const void* shift, const void* scale, void* y, floa
 size_t adaln_bwd_workspace_size(int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype) {
     if (check_shape(D, dtype) || Bt < 0 || N < 0) return 0;
     if (N > 0 && Bt > INT64_MAX / N) return 0;
-    int sms = 0;
-    const int64_t G = bwd_tiles(Bt * N, D, false, dtype, &sms);
+    const int64_t G = bwd_tiles(Bt * N, D, false, dtype);
     if (G < 0) return 0;
     return bwd_need(G, Bt, D);
 }
@@ -310,8 +362,7 @@ int adaln_fwd_varlen(const void* x, const void* shift, const void* scale, void* 
 size_t adaln_bwd_varlen_workspace_size(int64_t total_tokens, int32_t nseg, int64_t nmod,
                                        int64_t D, adaln_dtype dtype) {
     if (check_shape(D, dtype) || total_tokens < 0 || nseg < 0 || nmod < 0) return 0;
-    int sms = 0;
-    const int64_t G = bwd_tiles(total_tokens, D, true, dtype, &sms);
+    const int64_t G = bwd_tiles(total_tokens, D, true, dtype);
     if (G < 0) return 0;
     return bwd_need(G, nseg, D);
 }

@@ -10,163 +10,235 @@
 // column accumulators. At the end of each (tile, segment) piece the accumulators are
 // written as one fp32 partial; stage 2 sums the partials of each modulation row in a
 // fixed order. No float atomics; dy and x are read from HBM exactly once.
+//
+// As in the forward, the ring variant streams each thread's vectors of x and dy (and the
+// rows' saved mean/rstd) `stages - 1` rounds ahead into shared memory with per-thread
+// cp.async, and the elementwise math runs on fp32 pairs.
 #include "common.cuh"
 #include "launch.h"
 
 namespace adaln {
 
-template <typename T, int NV, bool VARLEN>
+template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
 __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const BwdArgs a) {
     using IO = Io<T>;
     constexpr int VE = IO::VE;
+    constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector
     constexpr int RB = RowShape<NV>::kRows;
-    __shared__ float red[2][RB][2][32];   // double-buffered per-warp sums of g and g*xhat
+    extern __shared__ uint4 ring[];
+    __shared__ __align__(16) float red[2][2 * RB][32];  // double-buffered per-warp sums of g, g*xhat
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = blockDim.x >> 5;
+    const int TPB = blockDim.x;
+    const int nwarps = TPB >> 5, nquads = (nwarps + 3) >> 2;
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t R = a.seg.R, D = a.D, V = D / VE;
     const int64_t r0 = tile_begin(b, R, G), r1 = tile_begin(b + 1, R, G);
-    const T* __restrict__ x = static_cast<const T*>(a.x);
-    const T* __restrict__ dy = static_cast<const T*>(a.dy);
-    T* __restrict__ dx = static_cast<T*>(a.dx);
+    const char* __restrict__ xb = static_cast<const char*>(a.x);
+    const char* __restrict__ gb = static_cast<const char*>(a.dy);
+    char* __restrict__ dxb = static_cast<char*>(a.dx);
+    const int64_t row_bytes = D * (int64_t)sizeof(T);
     const float invD = 1.0f / (float)D;
+    const int ns = a.stages;
 
+    // Ring layout (32-bit shared addresses): [ns][RB][x, dy] rows of NV*TPB vectors, then
+    // [ns][RB][mean, rstd] one word per thread, so the saved statistics arrive with the rows
+    // instead of on the round's critical path.
+    const uint32_t vk = (uint32_t)TPB * 16u;
+    const uint32_t vrow = (uint32_t)NV * vk;           // one tensor's row
+    const uint32_t vslot = (uint32_t)RB * 2u * vrow;   // one round: RB rows of x and dy
+    const uint32_t ring_sa = smem_addr(ring);
+    const uint32_t my_vec = ring_sa + (uint32_t)tid * 16u;
+    const uint32_t my_st = ring_sa + (uint32_t)ns * vslot + (uint32_t)tid * 4u;
+    const uint32_t strow = (uint32_t)TPB * 8u, stslot = (uint32_t)RB * strow;
+
+    zero_absent_warps<2 * RB>(red[0], nwarps);
+    zero_absent_warps<2 * RB>(red[1], nwarps);
     uint32_t err = validate_segments<VARLEN>(a.seg, b, G);
 
-    int64_t col[NV];
+    uint32_t colb[NV];
     bool ok[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        const int64_t v = tid + (int64_t)k * blockDim.x;
-        ok[k] = v < V;
-        col[k] = v * VE;
+        const int64_t v = tid + (int64_t)k * TPB;
+        ok[k] = FULL || v < V;
+        colb[k] = (uint32_t)(v * 16);
     }
 
-    int buf = 0;
-    int64_t row = r0;
-    int64_t s = R > 0 ? seg_find<VARLEN>(a.seg, r0) : 0;
-    while (row < r1) {
-        while (s < a.seg.nseg && seg_start<VARLEN>(a.seg, s + 1) <= row) ++s;
-        if (s >= a.seg.nseg) {
-            err |= kErrSeqlens;
-            break;
-        }
-        const int64_t pend = min(seg_start<VARLEN>(a.seg, s + 1), r1);
-        const int64_t m = seg_mod<VARLEN>(a.seg, s);
-        if (m < 0 || m >= a.seg.nmod) {
-            err |= kErrModIdx;
-            row = pend;
-            continue;
-        }
-        float sc1[NV][VE];
-        float acc_dy[NV][VE], acc_dyx[NV][VE];
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            uint4 vc = make_uint4(0, 0, 0, 0);
-            if (ok[k]) vc = ld_keep(static_cast<const T*>(a.scale) + m * D + col[k]);
-            IO::unpack(vc, sc1[k]);
-#pragma unroll
-            for (int j = 0; j < VE; ++j) {
-                sc1[k][j] += 1.0f;
-                acc_dy[k][j] = 0.0f;
-                acc_dyx[k][j] = 0.0f;
-            }
-        }
+    const int64_t s0 = R > 0 ? seg_find<VARLEN>(a.seg, r0) : 0;
+    Walker<VARLEN, RB> cw{r0, s0, -1, false};
+    Walker<VARLEN, RB> pw{r0, s0, -1, false};
 
-        while (row < pend) {
-            const int nr = (int)min((int64_t)RB, pend - row);
-            uint4 xv[RB][NV], gv[RB][NV];
-            float mu[RB], rs[RB];
+    auto prefetch = [&](int slot) {
+        int64_t rs, sg;
+        int nr;
+        if (pw.next(a.seg, r1, rs, nr, sg)) {
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                const bool live = i < nr;
-                mu[i] = live ? __ldg(a.mean + row + i) : 0.0f;
-                rs[i] = live ? __ldg(a.rstd + row + i) : 0.0f;
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const bool on = live && ok[k];
-                    xv[i][k] = on ? ld_stream(x + (row + i) * D + col[k]) : make_uint4(0, 0, 0, 0);
-                    gv[i][k] = on ? ld_stream(dy + (row + i) * D + col[k]) : make_uint4(0, 0, 0, 0);
-                }
-            }
-            // Row sums of g and g*xhat; column sums of dy and dy*xhat.
-            float sums[2 * RB];
-#pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                float sg = 0.0f, sgx = 0.0f;
+                if (i >= nr) continue;
+                const uint32_t xd = my_vec + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
+                const uint32_t st = my_st + (uint32_t)slot * stslot + (uint32_t)i * strow;
+                const int64_t off = (rs + i) * row_bytes;
+                cp_async4_sa(st, a.mean + rs + i);
+                cp_async4_sa(st + (uint32_t)TPB * 4u, a.rstd + rs + i);
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     if (!ok[k]) continue;
-                    float fx[VE], fd[VE];
-                    IO::unpack(xv[i][k], fx);
-                    IO::unpack(gv[i][k], fd);
+                    cp_async16_sa(xd + (uint32_t)k * vk, xb + off + colb[k]);
+                    cp_async16_sa(xd + vrow + (uint32_t)k * vk, gb + off + colb[k]);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    if constexpr (RING) {
+        for (int q = 0; q < ns; ++q) prefetch(q);
+    }
+
+    int slot = 0, buf = 0;
+    int64_t cur_s = -1;
+    bool cur_ok = false;
+    float2 sc1[NV][PV];
+    float2 acc_dy[NV][PV], acc_dyx[NV][PV];
 #pragma unroll
-                    for (int j = 0; j < VE; ++j) {
-                        const float xhat = (fx[j] - mu[i]) * rs[i];
-                        const float g = fd[j] * sc1[k][j];
-                        sg += g;
-                        sgx = fmaf(g, xhat, sgx);
-                        if (i < nr) {
-                            acc_dy[k][j] += fd[j];
-                            acc_dyx[k][j] = fmaf(fd[j], xhat, acc_dyx[k][j]);
-                        }
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int p = 0; p < PV; ++p) acc_dy[k][p] = acc_dyx[k][p] = f2(0.0f);
+
+    // Piece (tile b, segment cur_s) done: one fp32 partial row pair in slot b + cur_s.
+    auto flush = [&]() {
+        float* P = a.partials + (b + cur_s) * 2 * D;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            if (ok[k]) {
+                float* pk = P + colb[k] / sizeof(T);  // element offset of my vector k
+#pragma unroll
+                for (int p = 0; p < PV; p += 2) {
+                    *reinterpret_cast<float4*>(pk + 2 * p) =
+                        make_float4(acc_dy[k][p].x, acc_dy[k][p].y, acc_dy[k][p + 1].x, acc_dy[k][p + 1].y);
+                    *reinterpret_cast<float4*>(pk + D + 2 * p) = make_float4(
+                        acc_dyx[k][p].x, acc_dyx[k][p].y, acc_dyx[k][p + 1].x, acc_dyx[k][p + 1].y);
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < PV; ++p) acc_dy[k][p] = acc_dyx[k][p] = f2(0.0f);
+        }
+    };
+
+    int64_t row, s;
+    int nr;
+    while (cw.next(a.seg, r1, row, nr, s)) {
+        uint4 xv[RB][NV], gv[RB][NV];
+        float mu[RB], rs[RB];
+        if constexpr (RING) {
+            cp_async_wait(ns - 1);
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const uint32_t xs = my_vec + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const bool on = i < nr && ok[k];
+                    xv[i][k] = on ? lds128(xs + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                    gv[i][k] = on ? lds128(xs + vrow + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                }
+                const uint32_t st = my_st + (uint32_t)slot * stslot + (uint32_t)i * strow;
+                mu[i] = i < nr ? __uint_as_float(lds32(st)) : 0.0f;
+                rs[i] = i < nr ? __uint_as_float(lds32(st + (uint32_t)TPB * 4u)) : 0.0f;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const int64_t off = (row + i) * row_bytes;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const bool on = i < nr && ok[k];
+                    xv[i][k] = on ? ld_stream(xb + off + colb[k]) : make_uint4(0, 0, 0, 0);
+                    gv[i][k] = on ? ld_stream(gb + off + colb[k]) : make_uint4(0, 0, 0, 0);
+                }
+                mu[i] = i < nr ? __ldg(a.mean + row + i) : 0.0f;
+                rs[i] = i < nr ? __ldg(a.rstd + row + i) : 0.0f;
+            }
+        }
+
+        if (s != cur_s) {
+            if (cur_ok) flush();
+            cur_s = s;
+            const int64_t m = seg_mod<VARLEN>(a.seg, s);
+            cur_ok = m >= 0 && m < a.seg.nmod;
+            if (!cur_ok) err |= kErrModIdx;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                uint4 vc = make_uint4(0, 0, 0, 0);
+                if (cur_ok && ok[k]) vc = ld_keep(static_cast<const char*>(a.scale) + m * row_bytes + colb[k]);
+                IO::unpack2(vc, sc1[k]);
+#pragma unroll
+                for (int p = 0; p < PV; ++p) sc1[k][p] = f2_add(sc1[k][p], f2(1.0f));
+            }
+        }
+
+        if (cur_ok) {  // uniform across the CTA
+            // xhat = (x - mean) * rstd, g = dy * (1 + scale); row sums of g and g*xhat;
+            // column sums of dy and dy*xhat. Rows past nr and idle lanes load dy = 0, so they
+            // add nothing anywhere.
+            float2 xh[RB][NV][PV], g[RB][NV][PV];
+            float sums[2 * RB];
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const float2 rs2 = f2(rs[i]), mu2 = f2(mu[i]);
+                float2 sg = f2(0.0f), sgx = f2(0.0f);
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    float2 fd[PV];
+                    IO::unpack2(xv[i][k], xh[i][k]);
+                    IO::unpack2(gv[i][k], fd);
+#pragma unroll
+                    for (int p = 0; p < PV; ++p) {
+                        // x - mean first: exact for rows whose mean dwarfs their spread.
+                        xh[i][k][p] = f2_mul(f2_sub(xh[i][k][p], mu2), rs2);
+                        g[i][k][p] = f2_mul(fd[p], sc1[k][p]);
+                        sg = f2_add(sg, g[i][k][p]);
+                        sgx = f2_fma(g[i][k][p], xh[i][k][p], sgx);
+                        acc_dy[k][p] = f2_add(acc_dy[k][p], fd[p]);
+                        acc_dyx[k][p] = f2_fma(fd[p], xh[i][k][p], acc_dyx[k][p]);
                     }
                 }
-                sums[2 * i] = sg;
-                sums[2 * i + 1] = sgx;
+                sums[2 * i] = sg.x + sg.y;
+                sums[2 * i + 1] = sgx.x + sgx.y;
             }
             warp_sum(sums);
             if (lane == 0) {
 #pragma unroll
-                for (int i = 0; i < RB; ++i) {
-                    red[buf][i][0][warp] = sums[2 * i];
-                    red[buf][i][1][warp] = sums[2 * i + 1];
-                }
+                for (int i = 0; i < 2 * RB; ++i) red[buf][i][warp] = sums[i];
             }
             __syncthreads();
+            cta_sum(red[buf], nquads, sums);
+            // dx = rstd * (g - mean(g) - xhat * mean(g*xhat))
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 if (i >= nr) continue;
-                float tg = 0.0f, tgx = 0.0f;
-                for (int w = 0; w < nwarps; ++w) {
-                    tg += red[buf][i][0][w];
-                    tgx += red[buf][i][1][w];
-                }
-                const float mg = tg * invD, mgx = tgx * invD;
-                T* dxr = dx + (row + i) * D;
+                const float mg = sums[2 * i] * invD, mgx = sums[2 * i + 1] * invD;
+                const float2 rs2 = f2(rs[i]), nmgx = f2(-mgx), nmgr = f2(-mg * rs[i]);
+                char* dxr = dxb + (row + i) * row_bytes;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     if (!ok[k]) continue;
-                    float fx[VE], fd[VE];
-                    IO::unpack(xv[i][k], fx);
-                    IO::unpack(gv[i][k], fd);
+                    float2 o[PV];
 #pragma unroll
-                    for (int j = 0; j < VE; ++j) {
-                        const float xhat = (fx[j] - mu[i]) * rs[i];
-                        const float g = fd[j] * sc1[k][j];
-                        fd[j] = rs[i] * (g - mg - xhat * mgx);
-                    }
-                    st_vec(dxr + col[k], IO::pack(fd));
+                    for (int p = 0; p < PV; ++p)
+                        o[p] = f2_fma(f2_fma(xh[i][k][p], nmgx, g[i][k][p]), rs2, nmgr);
+                    st_vec(dxr + colb[k], IO::pack2v(o));
                 }
             }
             buf ^= 1;
-            row += nr;
         }
-        // Piece (tile b, segment s) done: one fp32 partial row pair in slot b + s.
-        float* P = a.partials + (b + s) * 2 * D;
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            if (!ok[k]) continue;
-#pragma unroll
-            for (int j = 0; j < VE; j += 4) {
-                *reinterpret_cast<float4*>(P + col[k] + j) =
-                    make_float4(acc_dy[k][j], acc_dy[k][j + 1], acc_dy[k][j + 2], acc_dy[k][j + 3]);
-                *reinterpret_cast<float4*>(P + D + col[k] + j) = make_float4(
-                    acc_dyx[k][j], acc_dyx[k][j + 1], acc_dyx[k][j + 2], acc_dyx[k][j + 3]);
-            }
+        if constexpr (RING) {
+            prefetch(slot);
+            slot = slot + 1 == ns ? 0 : slot + 1;
         }
     }
+    if (cur_ok) flush();
+    if (cw.bad) err |= kErrSeqlens;
+    if constexpr (RING) cp_async_wait_all();
     publish_status(err, a.status, a.header);
 }
 
@@ -254,39 +326,53 @@ __global__ void __launch_bounds__(kStage2Threads) stage2_kernel(const Stage2Args
     }
 }
 
-template <typename T, int NV, bool VARLEN>
+template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
 static const void* bwd_fn() {
-    return reinterpret_cast<const void*>(&bwd_kernel<T, NV, VARLEN>);
+    return reinterpret_cast<const void*>(&bwd_kernel<T, NV, VARLEN, RING, FULL>);
 }
 
-static const void* pick_bwd(int dtype, int nv, bool varlen) {
-#define ADALN_PICK(T)                                                            \
-    switch (nv) {                                                                \
-        case 1: return varlen ? bwd_fn<T, 1, true>() : bwd_fn<T, 1, false>();     \
-        case 2: return varlen ? bwd_fn<T, 2, true>() : bwd_fn<T, 2, false>();     \
-        case 3: return varlen ? bwd_fn<T, 3, true>() : bwd_fn<T, 3, false>();     \
-        case 4: return varlen ? bwd_fn<T, 4, true>() : bwd_fn<T, 4, false>();     \
-        default: return nullptr;                                                 \
+// Instantiated variants: ring + full row, ring + partial row, plain (partial row).
+template <typename T, int NV, bool VARLEN>
+static const void* pick_variant(bool ring, bool full) {
+    if (ring) return full ? bwd_fn<T, NV, VARLEN, true, true>() : bwd_fn<T, NV, VARLEN, true, false>();
+    return bwd_fn<T, NV, VARLEN, false, false>();
+}
+
+template <typename T, bool VARLEN>
+static const void* pick_nv(int nv, bool ring, bool full) {
+    switch (nv) {
+        case 1: return pick_variant<T, 1, VARLEN>(ring, full);
+        case 2: return pick_variant<T, 2, VARLEN>(ring, full);
+        case 4: return pick_variant<T, 4, VARLEN>(ring, full);
+        case 8: return pick_variant<T, 8, VARLEN>(ring, full);
+        default: return nullptr;
     }
-    if (dtype == 0) { ADALN_PICK(float) }
-    if (dtype == 1) { ADALN_PICK(__nv_bfloat16) }
-#undef ADALN_PICK
+}
+
+static const void* pick_bwd(int dtype, int nv, bool varlen, bool ring, bool full) {
+    if (dtype == 0) return varlen ? pick_nv<float, true>(nv, ring, full) : pick_nv<float, false>(nv, ring, full);
+    if (dtype == 1)
+        return varlen ? pick_nv<__nv_bfloat16, true>(nv, ring, full)
+                      : pick_nv<__nv_bfloat16, false>(nv, ring, full);
     return nullptr;
 }
 
-cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, int tpb, int* out) {
-    const void* fn = pick_bwd(dtype, nv, varlen);
+cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
+                              size_t smem, int* out) {
+    const void* fn = pick_bwd(dtype, nv, varlen, ring, full);
     if (!fn) return cudaErrorInvalidValue;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, fn, tpb, 0);
+    cudaError_t e = allow_dynamic_smem(fn);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, fn, tpb, smem);
 }
 
-cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, int64_t G, int tpb,
-                       cudaStream_t stream) {
-    const void* fn = pick_bwd(dtype, nv, varlen);
+cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
+                       int64_t G, int tpb, size_t smem, cudaStream_t stream) {
+    const void* fn = pick_bwd(dtype, nv, varlen, ring, full);
     if (!fn) return cudaErrorInvalidValue;
     BwdArgs a = args;
     void* params[] = {&a};
-    return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, 0, stream);
+    return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream);
 }
 
 cudaError_t launch_stage2(const Stage2Args& args, bool varlen, cudaStream_t stream) {

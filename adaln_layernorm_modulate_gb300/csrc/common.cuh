@@ -10,14 +10,15 @@ namespace adaln {
 
 constexpr int kMaxCtas = 4096;      // upper bound on the row-tile count of one launch
 constexpr int kStage2Threads = 256;
+constexpr int kMaxStages = 8;       // deepest shared-memory ring, in rounds
 
-// A CTA processes one row at a time (or kRows rows per reduction round), each thread owning
-// NV 16-byte column vectors of the row. Wider rows hold fewer rows per round so the
-// accumulators stay in registers; kMaxThreads bounds the CTA size the host may pick.
+// A CTA processes its rows in rounds of kRows rows, each thread owning NV 16-byte column
+// vectors of every row. Wider per-thread slices hold fewer rows per round so the values
+// stay in registers; kMaxThreads bounds the CTA size the host may pick for that NV.
 template <int NV>
 struct RowShape {
-    static constexpr int kRows = NV >= 3 ? 1 : 2;
-    static constexpr int kMaxThreads = NV >= 4 ? 1024 : 512;
+    static constexpr int kRows = NV <= 2 ? 2 : 1;
+    static constexpr int kMaxThreads = NV == 1 || NV >= 8 ? 512 : 384;
 };
 
 // Workspace layout: [header | one status word per CTA | backward partials].
@@ -57,6 +58,7 @@ struct FwdArgs {
     Segments seg;
     uint32_t* status;    // per-CTA status words (packed calls), or null
     WsHeader* header;
+    int stages;          // shared-memory ring depth in rounds (ring kernels only)
 };
 
 struct BwdArgs {
@@ -71,6 +73,7 @@ struct BwdArgs {
     Segments seg;
     uint32_t* status;
     WsHeader* header;
+    int stages;
 };
 
 struct Stage2Args {
@@ -158,6 +161,184 @@ __device__ __forceinline__ void publish_status(uint32_t err, uint32_t* words, Ws
 }
 
 // ---------------------------------------------------------------------------------------
+// Rounds: a CTA walks its tile in rounds of up to RB consecutive rows that never cross a
+// segment boundary. Two walkers with the same start produce the same sequence, so a
+// prefetching walker can run ahead of the consuming one.
+// ---------------------------------------------------------------------------------------
+template <bool VARLEN, int RB>
+struct Walker {
+    int64_t row;      // first row of the next round
+    int64_t s;        // segment holding `row` once seg_end is valid
+    int64_t seg_end;  // min(end of segment s, tile end); -1 before the first round
+    bool bad;         // ran past the segment table
+
+    __device__ __forceinline__ bool next(const Segments& sg, int64_t r1, int64_t& start, int& nr,
+                                         int64_t& seg) {
+        if (row >= r1) return false;
+        if (row >= seg_end) {
+            while (s < sg.nseg && seg_start<VARLEN>(sg, s + 1) <= row) ++s;
+            if (s >= sg.nseg) {
+                bad = true;
+                row = r1;
+                return false;
+            }
+            seg_end = min(seg_start<VARLEN>(sg, s + 1), r1);
+        }
+        start = row;
+        nr = (int)min((int64_t)RB, seg_end - row);
+        seg = s;
+        row += nr;
+        return true;
+    }
+};
+
+// Asynchronous global -> shared copies issued per thread. Completion is tracked per thread
+// with commit/wait groups and each thread reads back only what it copied itself, so no
+// cross-thread synchronisation (and no waiting on anyone else) is involved.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+// 4-byte copy through L1 (the threads of a CTA fetch the same word: one L1 line).
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+// The same copies addressed by 32-bit shared-window addresses (cheaper index math).
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16_sa(uint32_t sa, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4_sa(uint32_t sa, const void* gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+// Shared loads issued after a cp.async wait: volatile, so they stay behind the wait.
+__device__ __forceinline__ uint4 lds128(uint32_t sa) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(sa));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t sa) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(sa));
+    return v;
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most n of this thread's groups are pending (n = ring depth - 1, 0..7).
+__device__ __forceinline__ void cp_async_wait(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Lets `fn` use, with its static shared memory, up to the device's opt-in shared memory per
+// block (host side).
+inline cudaError_t allow_dynamic_smem(const void* fn) {
+    int dev = 0, optin = 0;
+    cudaFuncAttributes attr{};
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&attr, fn);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - (int)attr.sharedSizeBytes);
+    return e;
+}
+
+// ---------------------------------------------------------------------------------------
+// Packed fp32 pairs: Blackwell's f32x2 ALU instructions. Each lane of a pair is rounded
+// exactly as the scalar instruction would round it.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+// ---------------------------------------------------------------------------------------
+// Reductions
+// ---------------------------------------------------------------------------------------
+// Butterfly sum over the warp: every lane ends with the same bits.
+template <int NVAL>
+__device__ __forceinline__ void warp_sum(float (&v)[NVAL]) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+        for (int i = 0; i < NVAL; ++i) v[i] += __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
+    }
+}
+
+// CTA-wide sum of one value per warp, written by lane 0 of each warp to red[i][warp]; the
+// slots of absent warps (warp >= nwarps) hold zeros. Every thread reads the slots as float4s
+// and adds them in the same fixed order, so all threads of the CTA get the same bits.
+template <int NVAL>
+__device__ __forceinline__ void cta_sum(const float (*red)[32], int nquads, float (&out)[NVAL]) {
+#pragma unroll
+    for (int i = 0; i < NVAL; ++i) {
+        float t = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // at most 16 warps a CTA
+            if (q < nquads) {
+                const float4 v = *reinterpret_cast<const float4*>(&red[i][4 * q]);
+                t += (v.x + v.y) + (v.z + v.w);
+            }
+        }
+        out[i] = t;
+    }
+}
+
+// Zero the reduction slots no warp writes (called once, before the first barrier).
+template <int NROWS>
+__device__ __forceinline__ void zero_absent_warps(float (*red)[32], int nwarps) {
+    for (int idx = threadIdx.x; idx < NROWS * 32; idx += blockDim.x)
+        if ((idx & 31) >= nwarps) red[idx >> 5][idx & 31] = 0.0f;
+}
+
+// ---------------------------------------------------------------------------------------
 // 16-byte vectors of the I/O type.
 // ---------------------------------------------------------------------------------------
 template <typename T>
@@ -166,45 +347,45 @@ struct Io;
 template <>
 struct Io<float> {
     static constexpr int VE = 4;  // elements per 16-byte vector
-    __device__ static __forceinline__ void unpack(const uint4& v, float* f) {
-        f[0] = __uint_as_float(v.x);
-        f[1] = __uint_as_float(v.y);
-        f[2] = __uint_as_float(v.z);
-        f[3] = __uint_as_float(v.w);
+    // As VE/2 fp32 pairs (element 2p in .x, 2p+1 in .y).
+    __device__ static __forceinline__ void unpack2(const uint4& v, float2* f) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
     }
-    __device__ static __forceinline__ uint4 pack(const float* f) {
-        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                          __float_as_uint(f[3]));
+    __device__ static __forceinline__ uint4 pack2v(const float2* f) {
+        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                          __float_as_uint(f[1].y));
     }
     __device__ static __forceinline__ float first(const void* p) {
         return __ldg(reinterpret_cast<const float*>(p));
     }
+    // Element 0 of a row, from the row's first 32-bit word.
+    __device__ static __forceinline__ float first_of_word(uint32_t w) { return __uint_as_float(w); }
 };
 
 template <>
 struct Io<__nv_bfloat16> {
     static constexpr int VE = 8;
     // bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 pattern.
-    __device__ static __forceinline__ void unpack(const uint4& v, float* f) {
+    __device__ static __forceinline__ void unpack2(const uint4& v, float2* f) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = __uint_as_float(w[j] << 16);
-            f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
+        for (int j = 0; j < 4; ++j)
+            f[j] = make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
     }
-    __device__ static __forceinline__ uint32_t pack2(float lo, float hi) {
+    __device__ static __forceinline__ uint32_t pack_pair(float lo, float hi) {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
         return *reinterpret_cast<uint32_t*>(&h);
     }
-    __device__ static __forceinline__ uint4 pack(const float* f) {
-        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
-                          pack2(f[6], f[7]));
+    __device__ static __forceinline__ uint4 pack2v(const float2* f) {
+        return make_uint4(pack_pair(f[0].x, f[0].y), pack_pair(f[1].x, f[1].y),
+                          pack_pair(f[2].x, f[2].y), pack_pair(f[3].x, f[3].y));
     }
     __device__ static __forceinline__ float first(const void* p) {
         const uint32_t h = __ldg(reinterpret_cast<const unsigned short*>(p));
         return __uint_as_float(h << 16);
     }
+    __device__ static __forceinline__ float first_of_word(uint32_t w) { return __uint_as_float(w << 16); }
 };
 
 // Streamed (read-once) 16-byte load: read-only path, no L1 allocation.
@@ -223,15 +404,6 @@ __device__ __forceinline__ uint4 ld_keep(const void* p) {
 
 __device__ __forceinline__ void st_vec(void* p, const uint4& v) {
     *reinterpret_cast<uint4*>(p) = v;
-}
-
-template <int NVAL>
-__device__ __forceinline__ void warp_sum(float (&v)[NVAL]) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-#pragma unroll
-        for (int i = 0; i < NVAL; ++i) v[i] += __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
-    }
 }
 
 }  // namespace adaln

@@ -3,132 +3,196 @@
 // AdaptiveLoad technical summary, section 2.B, forward-pass bullet: mean and variance
 // are kept on chip and reduced by warp shuffles followed by a block reduction, and the
 // modulation is applied on a further pass over D. Here one CTA owns a contiguous tile of
-// rows; each thread owns the same 16-byte column vectors of every row, so the row is held
+// rows; each thread owns the same 16-byte column vectors of every row, so a row is held
 // in registers and the three passes (sum, centred sum of squares, modulated write) run
 // over registers, touching HBM once for x and once for y.
 //
+// Memory-level parallelism: in the ring variant every thread streams its own vectors of
+// the next `stages - 1` rounds into shared memory with cp.async while it works on the
+// current round (each thread reads back only what it copied, so the ring needs no
+// cross-thread synchronisation). The plain variant, used when a row is too wide for a
+// ring of two rounds, loads straight into registers. FULL: the CTA's threads cover the
+// row exactly (no idle vector slots), so no lane masking is needed.
+//
 // Variance: sum and centred sum of squares of d = x - x[row, 0]. Subtracting the row's
 // first element first (shifted data, Chan, Golub & LeVeque 1983) keeps the fp32 sums of
-// rows with a large mean and a tiny spread exact enough; the second pass is centred on
-// the mean of d (two-pass), never E[x^2] - E[x]^2.
+// rows with a large mean and a tiny spread accurate; the second pass is centred on the
+// mean of d (two-pass), never E[x^2] - E[x]^2. Elementwise math runs on fp32 pairs.
 #include "common.cuh"
 #include "launch.h"
 
 namespace adaln {
 
-template <typename T, int NV, bool VARLEN>
+template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
 __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const FwdArgs a) {
     using IO = Io<T>;
     constexpr int VE = IO::VE;
+    constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector
     constexpr int RB = RowShape<NV>::kRows;
-    __shared__ float red1[RB][32];
-    __shared__ float red2[RB][32];
+    extern __shared__ uint4 ring[];
+    __shared__ __align__(16) float red1[RB][32];
+    __shared__ __align__(16) float red2[RB][32];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = blockDim.x >> 5;
+    const int TPB = blockDim.x;
+    const int nwarps = TPB >> 5, nquads = (nwarps + 3) >> 2;
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t R = a.seg.R, D = a.D, V = D / VE;
     const int64_t r0 = tile_begin(b, R, G), r1 = tile_begin(b + 1, R, G);
-    const T* __restrict__ x = static_cast<const T*>(a.x);
-    T* __restrict__ y = static_cast<T*>(a.y);
+    const char* __restrict__ xb = static_cast<const char*>(a.x);
+    char* __restrict__ yb = static_cast<char*>(a.y);
+    const int64_t row_bytes = D * (int64_t)sizeof(T);
     const float invD = 1.0f / (float)D;
+    const int ns = a.stages;
 
+    // Ring layout (32-bit shared addresses): [ns][RB] rows of NV*TPB vectors, then [ns][RB]
+    // words of each row's element 0, one per thread (the row's shift point K, read without
+    // cross-thread synchronisation).
+    const uint32_t vk = (uint32_t)TPB * 16u;             // one vector index k across the CTA
+    const uint32_t vrow = (uint32_t)NV * vk;           // one row
+    const uint32_t vslot = (uint32_t)RB * vrow;        // one round
+    const uint32_t ring_sa = smem_addr(ring);
+    const uint32_t my_vec = ring_sa + (uint32_t)tid * 16u;
+    const uint32_t my_k = ring_sa + (uint32_t)ns * vslot + (uint32_t)tid * 4u;
+    const uint32_t krow = (uint32_t)TPB * 4u, kslot = (uint32_t)RB * krow;
+
+    zero_absent_warps<RB>(red1, nwarps);
+    zero_absent_warps<RB>(red2, nwarps);
     uint32_t err = validate_segments<VARLEN>(a.seg, b, G);
 
-    int64_t col[NV];
+    uint32_t colb[NV];  // byte offset of my vector k within a row
     bool ok[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        const int64_t v = tid + (int64_t)k * blockDim.x;
-        ok[k] = v < V;
-        col[k] = v * VE;
+        const int64_t v = tid + (int64_t)k * TPB;
+        ok[k] = FULL || v < V;
+        colb[k] = (uint32_t)(v * 16);
     }
 
-    int64_t row = r0;
-    int64_t s = R > 0 ? seg_find<VARLEN>(a.seg, r0) : 0;
-    while (row < r1) {
-        while (s < a.seg.nseg && seg_start<VARLEN>(a.seg, s + 1) <= row) ++s;
-        if (s >= a.seg.nseg) {
-            err |= kErrSeqlens;
-            break;
-        }
-        const int64_t pend = min(seg_start<VARLEN>(a.seg, s + 1), r1);
-        const int64_t m = seg_mod<VARLEN>(a.seg, s);
-        if (m < 0 || m >= a.seg.nmod) {
-            err |= kErrModIdx;
-            row = pend;
-            continue;
-        }
-        // This segment's modulation for my columns: shift and (1 + scale) in fp32.
-        float sh[NV][VE], sc1[NV][VE];
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            uint4 vs = make_uint4(0, 0, 0, 0), vc = make_uint4(0, 0, 0, 0);
-            if (ok[k]) {
-                vs = ld_keep(static_cast<const T*>(a.shift) + m * D + col[k]);
-                vc = ld_keep(static_cast<const T*>(a.scale) + m * D + col[k]);
-            }
-            IO::unpack(vs, sh[k]);
-            IO::unpack(vc, sc1[k]);
-#pragma unroll
-            for (int j = 0; j < VE; ++j) sc1[k][j] += 1.0f;
-        }
+    const int64_t s0 = R > 0 ? seg_find<VARLEN>(a.seg, r0) : 0;
+    Walker<VARLEN, RB> cw{r0, s0, -1, false};
+    Walker<VARLEN, RB> pw{r0, s0, -1, false};
 
-        while (row < pend) {
-            const int nr = (int)min((int64_t)RB, pend - row);
-            uint4 xv[RB][NV];
-            float K[RB];
+    // Copy this thread's vectors of the prefetch walker's next round into ring slot `slot`.
+    auto prefetch = [&](int slot) {
+        int64_t rs, sg;
+        int nr;
+        if (pw.next(a.seg, r1, rs, nr, sg)) {
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                const T* xr = x + (row + i) * D;
-                K[i] = (i < nr) ? IO::first(xr) : 0.0f;
+                if (i >= nr) continue;
+                const char* src = xb + (rs + i) * row_bytes;
+                const uint32_t dst = my_vec + (uint32_t)slot * vslot + (uint32_t)i * vrow;
+                cp_async4_sa(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow, src);
 #pragma unroll
                 for (int k = 0; k < NV; ++k)
-                    xv[i][k] = (i < nr && ok[k]) ? ld_stream(xr + col[k]) : make_uint4(0, 0, 0, 0);
+                    if (ok[k]) cp_async16_sa(dst + (uint32_t)k * vk, src + colb[k]);
             }
-            // Pass 1: sum of d = x - K.
+        }
+        cp_async_commit();
+    };
+    if constexpr (RING) {
+        for (int q = 0; q < ns; ++q) prefetch(q);
+    }
+
+    int slot = 0;
+    int64_t cur_s = -1;
+    bool cur_ok = false;
+    float2 sh[NV][PV], sc1[NV][PV];
+    int64_t row, s;
+    int nr;
+    while (cw.next(a.seg, r1, row, nr, s)) {
+        uint4 xv[RB][NV];
+        float K[RB];
+        if constexpr (RING) {
+            cp_async_wait(ns - 1);
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const uint32_t src = my_vec + (uint32_t)slot * vslot + (uint32_t)i * vrow;
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
+                    xv[i][k] = (i < nr && ok[k]) ? lds128(src + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                K[i] = (i < nr) ? IO::first_of_word(lds32(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow))
+                                : 0.0f;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const char* src = xb + (row + i) * row_bytes;
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
+                    xv[i][k] = (i < nr && ok[k]) ? ld_stream(src + colb[k]) : make_uint4(0, 0, 0, 0);
+                K[i] = (i < nr) ? IO::first(src) : 0.0f;
+            }
+        }
+
+        if (s != cur_s) {
+            // A new segment: its modulation for my columns, shift and (1 + scale) in fp32.
+            cur_s = s;
+            const int64_t m = seg_mod<VARLEN>(a.seg, s);
+            cur_ok = m >= 0 && m < a.seg.nmod;
+            if (!cur_ok) err |= kErrModIdx;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                uint4 vs = make_uint4(0, 0, 0, 0), vc = make_uint4(0, 0, 0, 0);
+                if (cur_ok && ok[k]) {
+                    vs = ld_keep(static_cast<const char*>(a.shift) + m * row_bytes + colb[k]);
+                    vc = ld_keep(static_cast<const char*>(a.scale) + m * row_bytes + colb[k]);
+                }
+                IO::unpack2(vs, sh[k]);
+                IO::unpack2(vc, sc1[k]);
+#pragma unroll
+                for (int p = 0; p < PV; ++p) sc1[k][p] = f2_add(sc1[k][p], f2(1.0f));
+            }
+        }
+
+        if (cur_ok) {  // uniform across the CTA
+            // d = x - K, kept for all three passes; idle lanes hold d = 0.
+            float2 d[RB][NV][PV];
             float s1[RB];
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                s1[i] = 0.0f;
+                float2 acc0 = f2(0.0f), acc1 = f2(0.0f);
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
-                    if (!ok[k]) continue;
-                    float f[VE];
-                    IO::unpack(xv[i][k], f);
+                    IO::unpack2(xv[i][k], d[i][k]);
 #pragma unroll
-                    for (int j = 0; j < VE; ++j) s1[i] += f[j] - K[i];
+                    for (int p = 0; p < PV; ++p) {
+                        d[i][k][p] = f2_sub(d[i][k][p], f2(K[i]));
+                        if (!FULL && !ok[k]) d[i][k][p] = f2(0.0f);
+                        if (p & 1) acc1 = f2_add(acc1, d[i][k][p]);
+                        else acc0 = f2_add(acc0, d[i][k][p]);
+                    }
                 }
+                const float2 acc = f2_add(acc0, acc1);
+                s1[i] = acc.x + acc.y;
             }
+            // Pass 1: mean of d.
             warp_sum(s1);
             if (lane == 0) {
 #pragma unroll
                 for (int i = 0; i < RB; ++i) red1[i][warp] = s1[i];
             }
             __syncthreads();
-            float md[RB];
-#pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                float t = 0.0f;
-                for (int w = 0; w < nwarps; ++w) t += red1[i][w];
-                md[i] = t * invD;
-            }
+            cta_sum(red1, nquads, s1);
             // Pass 2: centred sum of squares.
-            float s2[RB];
+            float s2[RB], md[RB];
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                s2[i] = 0.0f;
+                md[i] = s1[i] * invD;
+                float2 acc0 = f2(0.0f), acc1 = f2(0.0f);
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
-                    if (!ok[k]) continue;
-                    float f[VE];
-                    IO::unpack(xv[i][k], f);
 #pragma unroll
-                    for (int j = 0; j < VE; ++j) {
-                        const float c = (f[j] - K[i]) - md[i];
-                        s2[i] = fmaf(c, c, s2[i]);
+                    for (int p = 0; p < PV; ++p) {
+                        d[i][k][p] = f2_sub(d[i][k][p], f2(md[i]));
+                        if (!FULL && !ok[k]) d[i][k][p] = f2(0.0f);
+                        if (p & 1) acc1 = f2_fma(d[i][k][p], d[i][k][p], acc1);
+                        else acc0 = f2_fma(d[i][k][p], d[i][k][p], acc0);
                     }
                 }
+                const float2 acc = f2_add(acc0, acc1);
+                s2[i] = acc.x + acc.y;
             }
             warp_sum(s2);
             if (lane == 0) {
@@ -136,70 +200,85 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
                 for (int i = 0; i < RB; ++i) red2[i][warp] = s2[i];
             }
             __syncthreads();
-            // Pass 3: modulated write.
+            cta_sum(red2, nquads, s2);
+            // Pass 3: y = (d - mean_d) * rstd * (1 + scale) + shift.
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 if (i >= nr) continue;
-                float t = 0.0f;
-                for (int w = 0; w < nwarps; ++w) t += red2[i][w];
-                const float rs = rsqrtf(t * invD + a.eps);
-                T* yr = y + (row + i) * D;
+                const float rs = rsqrtf(s2[i] * invD + a.eps);
+                char* yr = yb + (row + i) * row_bytes;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     if (!ok[k]) continue;
-                    float f[VE];
-                    IO::unpack(xv[i][k], f);
+                    float2 o[PV];
 #pragma unroll
-                    for (int j = 0; j < VE; ++j) {
-                        const float xhat = ((f[j] - K[i]) - md[i]) * rs;
-                        f[j] = fmaf(xhat, sc1[k][j], sh[k][j]);
-                    }
-                    st_vec(yr + col[k], IO::pack(f));
+                    for (int p = 0; p < PV; ++p)
+                        o[p] = f2_fma(f2_mul(d[i][k][p], f2(rs)), sc1[k][p], sh[k][p]);
+                    st_vec(yr + colb[k], IO::pack2v(o));
                 }
                 if (tid == 0) {
                     a.mean[row + i] = K[i] + md[i];
                     a.rstd[row + i] = rs;
                 }
             }
-            row += nr;
+        }
+        if constexpr (RING) {
+            prefetch(slot);  // this slot's data is in registers: refill it `ns` rounds ahead
+            slot = slot + 1 == ns ? 0 : slot + 1;
         }
     }
+    if (cw.bad) err |= kErrSeqlens;
+    if constexpr (RING) cp_async_wait_all();
     publish_status(err, a.status, a.header);
 }
 
-template <typename T, int NV, bool VARLEN>
+template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
 static const void* fwd_fn() {
-    return reinterpret_cast<const void*>(&fwd_kernel<T, NV, VARLEN>);
+    return reinterpret_cast<const void*>(&fwd_kernel<T, NV, VARLEN, RING, FULL>);
 }
 
-static const void* pick_fwd(int dtype, int nv, bool varlen) {
-#define ADALN_PICK(T)                                                            \
-    switch (nv) {                                                                \
-        case 1: return varlen ? fwd_fn<T, 1, true>() : fwd_fn<T, 1, false>();     \
-        case 2: return varlen ? fwd_fn<T, 2, true>() : fwd_fn<T, 2, false>();     \
-        case 3: return varlen ? fwd_fn<T, 3, true>() : fwd_fn<T, 3, false>();     \
-        case 4: return varlen ? fwd_fn<T, 4, true>() : fwd_fn<T, 4, false>();     \
-        default: return nullptr;                                                 \
+// Instantiated variants: ring + full row, ring + partial row, plain (partial row).
+template <typename T, int NV, bool VARLEN>
+static const void* pick_variant(bool ring, bool full) {
+    if (ring) return full ? fwd_fn<T, NV, VARLEN, true, true>() : fwd_fn<T, NV, VARLEN, true, false>();
+    return fwd_fn<T, NV, VARLEN, false, false>();
+}
+
+template <typename T, bool VARLEN>
+static const void* pick_nv(int nv, bool ring, bool full) {
+    switch (nv) {
+        case 1: return pick_variant<T, 1, VARLEN>(ring, full);
+        case 2: return pick_variant<T, 2, VARLEN>(ring, full);
+        case 4: return pick_variant<T, 4, VARLEN>(ring, full);
+        case 8: return pick_variant<T, 8, VARLEN>(ring, full);
+        default: return nullptr;
     }
-    if (dtype == 0) { ADALN_PICK(float) }
-    if (dtype == 1) { ADALN_PICK(__nv_bfloat16) }
-#undef ADALN_PICK
+}
+
+static const void* pick_fwd(int dtype, int nv, bool varlen, bool ring, bool full) {
+    if (dtype == 0) return varlen ? pick_nv<float, true>(nv, ring, full) : pick_nv<float, false>(nv, ring, full);
+    if (dtype == 1)
+        return varlen ? pick_nv<__nv_bfloat16, true>(nv, ring, full)
+                      : pick_nv<__nv_bfloat16, false>(nv, ring, full);
     return nullptr;
 }
 
-cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, int tpb, int* out) {
-    const void* fn = pick_fwd(dtype, nv, varlen);
+cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
+                              size_t smem, int* out) {
+    const void* fn = pick_fwd(dtype, nv, varlen, ring, full);
     if (!fn) return cudaErrorInvalidValue;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, fn, tpb, 0);
+    cudaError_t e = allow_dynamic_smem(fn);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, fn, tpb, smem);
 }
 
-cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, int64_t G, int tpb,
-                       cudaStream_t stream) {
-    const void* fn = pick_fwd(dtype, nv, varlen);
+cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
+                       int64_t G, int tpb, size_t smem, cudaStream_t stream) {
+    const void* fn = pick_fwd(dtype, nv, varlen, ring, full);
     if (!fn) return cudaErrorInvalidValue;
     FwdArgs a = args;
     void* params[] = {&a};
-    return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, 0, stream);
+    return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream);
 }
 
 }  // namespace adaln

@@ -7,13 +7,17 @@
 
 namespace adaln {
 
-cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, int tpb, int* out);
-cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, int64_t G, int tpb,
-                       cudaStream_t stream);
+// `ring`: the cp.async shared-memory ring variant; `full`: the CTA covers the row exactly
+// (ring variant only); `smem`: the ring's dynamic shared memory bytes.
+cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
+                              size_t smem, int* out);
+cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
+                       int64_t G, int tpb, size_t smem, cudaStream_t stream);
 
-cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, int tpb, int* out);
-cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, int64_t G, int tpb,
-                       cudaStream_t stream);
+cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
+                              size_t smem, int* out);
+cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
+                       int64_t G, int tpb, size_t smem, cudaStream_t stream);
 cudaError_t launch_stage2(const Stage2Args& args, bool varlen, cudaStream_t stream);
 
 }  // namespace adaln

@@ -59,22 +59,40 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--max-tokens", type=int, default=0,
+                   help="keep only the leading segments holding at most this many tokens "
+                        "(a smaller case of the same workload, e.g. for profiler captures)")
     return p.parse_args()
 
 
 # ------------------------------------------------------------------------------------------
 # workload and byte accounting
 # ------------------------------------------------------------------------------------------
-def make_workload(name: str, bucket_batch=None, generate=True) -> synth.Workload:
+def make_workload(name: str, bucket_batch=None, generate=True, max_tokens=0) -> synth.Workload:
     spec = WORKLOADS[name]
     if spec == 3:
         if bucket_batch is None:
             import oracle
             bucket_batch = oracle.bucket_batch
-        return synth.config(3, bucket_batch=bucket_batch, generate=generate)
-    if isinstance(spec, tuple):
-        return synth.config(spec[0], dtype=spec[1], generate=generate)
-    return synth.config(spec, generate=generate)
+        w = synth.config(3, bucket_batch=bucket_batch, generate=False)
+    elif isinstance(spec, tuple):
+        w = synth.config(spec[0], dtype=spec[1], generate=False)
+    else:
+        w = synth.config(spec, generate=False)
+    if max_tokens and w.R > max_tokens:
+        keep = int(np.searchsorted(w.cu_seqlens, max_tokens, side="right")) - 1
+        if keep < 1:
+            raise ValueError("--max-tokens keeps no segment")
+        w.cu_seqlens = w.cu_seqlens[:keep + 1].copy()
+        w.mod_idx = w.mod_idx[:keep].copy()
+        w.nmod = int(w.mod_idx.max()) + 1
+        w.name += "-first%dtok" % w.R
+        if w.dense is not None:
+            w.dense = (keep, w.dense[1])
+        w.meta.pop("batches", None)
+    if generate:
+        synth.fill(w)
+    return w
 
 
 def describe(w: synth.Workload) -> dict:
@@ -256,7 +274,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, max_tokens=args.max_tokens)
     orc = oracle.get()
     per_row = oracle_rows_time(orc, w, 0, 64) / 64
     total_steps = args.steps + args.warmup
@@ -297,7 +315,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    w = make_workload(args.workload, bucket_batch=A.adaln_bucket_batch)
+    w = make_workload(args.workload, bucket_batch=A.adaln_bucket_batch, max_tokens=args.max_tokens)
     e = 2 if w.dtype == synth.BF16 else 4
     tdt = torch.bfloat16 if w.dtype == synth.BF16 else torch.float32
     packed = w.dense is None
