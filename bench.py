@@ -125,8 +125,7 @@ def hbm_peak():
 
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
-    for rel in ("adaln_layernorm_modulate_gb300/csrc/bwd.cu", "adaln_layernorm_modulate_gb300/csrc/common.cuh",
-                "adaln_layernorm_modulate_gb300/csrc/adaln.cu"):
+    for rel in ("adaln_layernorm_modulate_gb300/csrc/bwd.cu", "adaln_layernorm_modulate_gb300/csrc/common.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -259,7 +258,8 @@ def sample_bytes(w: synth.Workload, rows: int) -> int:
 def cpu_baseline(w: synth.Workload, seconds: float) -> dict:
     import oracle
     orc = oracle.get()
-    per_row = oracle_rows_time(orc, w, 0, 64) / 64
+    calib = min(w.R, 2048)
+    per_row = oracle_rows_time(orc, w, 0, calib) / calib
     rows = int(min(w.R, max(64, seconds / max(per_row, 1e-9))))
     dt = oracle_rows_time(orc, w, 0, rows)
     gbs = sample_bytes(w, rows) / dt / 1e9
