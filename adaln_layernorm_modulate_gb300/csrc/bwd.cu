@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 const float2 rs2 = f2(rs[i]), mu2 = f2(mu[i]);
-                float2 sg = f2(0.0f), sgx = f2(0.0f);
+                float2 sg[2] = {f2(0.0f), f2(0.0f)}, sgx[2] = {f2(0.0f), f2(0.0f)};
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     float2 fd[PV];
@@ -196,14 +196,15 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
                         // x - mean first: exact for rows whose mean dwarfs their spread.
                         xh[i][k][p] = f2_mul(f2_sub(xh[i][k][p], mu2), rs2);
                         g[i][k][p] = f2_mul(fd[p], sc1[k][p]);
-                        sg = f2_add(sg, g[i][k][p]);
-                        sgx = f2_fma(g[i][k][p], xh[i][k][p], sgx);
+                        sg[p & 1] = f2_add(sg[p & 1], g[i][k][p]);
+                        sgx[p & 1] = f2_fma(g[i][k][p], xh[i][k][p], sgx[p & 1]);
                         acc_dy[k][p] = f2_add(acc_dy[k][p], fd[p]);
                         acc_dyx[k][p] = f2_fma(fd[p], xh[i][k][p], acc_dyx[k][p]);
                     }
                 }
-                sums[2 * i] = sg.x + sg.y;
-                sums[2 * i + 1] = sgx.x + sgx.y;
+                const float2 tg = f2_add(sg[0], sg[1]), tgx = f2_add(sgx[0], sgx[1]);
+                sums[2 * i] = tg.x + tg.y;
+                sums[2 * i + 1] = tgx.x + tgx.y;
             }
             warp_sum(sums);
             if (lane == 0) {
