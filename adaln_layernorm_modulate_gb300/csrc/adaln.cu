@@ -2,6 +2,7 @@
 #include "adaln.h"
 
 #include <cmath>
+#include <cstdlib>
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -50,12 +51,21 @@ struct RowCfg {
 int max_threads_for(int nv) { return nv == 1 || nv >= 8 ? 512 : 384; }
 
 RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
-    static const int kNv[] = {1, 2, 4, 8};
+    static const int kNv[] = {1, 2, 3, 4, 6, 8};
     const int64_t VE = dtype == ADALN_BF16 ? 8 : 4;
     const int64_t V = D / VE;
     int64_t target = (forward ? 32 : 16) / VE;
     if ((V + 31) / 32 < target) target = (V + 31) / 32;
     if (target < 1) target = 1;
+    // First choice: a mapping that covers the row exactly (whole warps, no idle lanes),
+    // with nv as close to the target as possible (ties go to the smaller nv).
+    int best = 0;
+    for (int nv : kNv) {
+        if (V % nv != 0 || (V / nv) % 32 != 0 || V / nv > max_threads_for(nv)) continue;
+        if (nv > 2 * target) continue;
+        if (best == 0 || std::llabs(nv - target) < std::llabs(best - target)) best = nv;
+    }
+    if (best != 0) return RowCfg{best, (int)(V / best), true};
     for (int nv : kNv) {
         if (nv < target) continue;
         const int64_t tpb = ((V + nv - 1) / nv + 31) / 32 * 32;

@@ -344,7 +344,9 @@ static const void* pick_nv(int nv, bool ring, bool full) {
     switch (nv) {
         case 1: return pick_variant<T, 1, VARLEN>(ring, full);
         case 2: return pick_variant<T, 2, VARLEN>(ring, full);
+        case 3: return pick_variant<T, 3, VARLEN>(ring, full);
         case 4: return pick_variant<T, 4, VARLEN>(ring, full);
+        case 6: return pick_variant<T, 6, VARLEN>(ring, full);
         case 8: return pick_variant<T, 8, VARLEN>(ring, full);
         default: return nullptr;
     }
