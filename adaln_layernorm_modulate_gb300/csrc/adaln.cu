@@ -19,7 +19,7 @@ constexpr int kMaxDevices = 64;
 
 std::mutex g_mu;
 int g_sms[kMaxDevices];  // 0 = not yet queried
-std::map<std::tuple<int, int, int, int, int, int>, int> g_occupancy;
+std::map<std::tuple<int, int, int, int, int, int>, std::pair<int, int>> g_plans;  // launch plans
 
 // Multiprocessor count of the current device (cached), or 0 on failure.
 int current_sms(int* dev_out) {
@@ -77,7 +77,8 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
 
 enum Kind { kFwd = 0, kBwd = 1 };
 
-// Shared memory a CTA may give its cp.async ring: two such CTAs fit on one SM.
+// Most shared memory a CTA gives its cp.async ring (two such CTAs fit on one SM); less when
+// registers let more CTAs share the SM.
 constexpr size_t kRingBudget = 100 * 1024;
 
 struct Plan {
@@ -108,31 +109,46 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
     p->sms = sms;
     p->c = row_cfg(D, dtype, kind == kFwd);
     const size_t round = ring_round_bytes(kind, p->c);
-    size_t stages = kRingBudget / round;
-    if (stages > (size_t)kMaxStages) stages = kMaxStages;
-    p->ring = stages >= 2;
+    p->ring = kRingBudget / round >= 2;
     p->full = p->ring && p->c.full;
-    p->stages = p->ring ? (int)stages : 0;
-    p->smem = p->ring ? stages * round : 0;
     const auto key = std::make_tuple(dev, (int)kind, (int)dtype, p->c.nv,
-                                     (int)varlen * 4 + (int)p->ring * 2 + (int)p->full,
-                                     p->c.tpb * 16 + p->stages);
-    int bps = 0;
+                                     (int)varlen * 4 + (int)p->ring * 2 + (int)p->full, p->c.tpb);
+    std::pair<int, int> cached{0, 0};  // (stages, CTAs per SM)
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        auto it = g_occupancy.find(key);
-        if (it != g_occupancy.end()) bps = it->second;
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) cached = it->second;
     }
-    if (bps == 0) {
-        const cudaError_t e =
-            kind == kFwd
-                ? fwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring, p->full, p->c.tpb, p->smem, &bps)
-                : bwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring, p->full, p->c.tpb, p->smem, &bps);
-        if (e != cudaSuccess || bps <= 0) return false;
+    if (cached.second == 0) {
+        auto occupancy = [&](size_t smem, int* bps) {
+            return kind == kFwd
+                       ? fwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring, p->full, p->c.tpb, smem, bps)
+                       : bwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring, p->full, p->c.tpb, smem, bps);
+        };
+        int stages = 0, bps = 0;
+        if (p->ring) {
+            // Size the ring so shared memory does not cut the residency registers allow:
+            // the SM's shared memory is split among the CTAs the registers let in.
+            int by_regs = 0, sm_bytes = 0;
+            if (occupancy(0, &by_regs) != cudaSuccess || by_regs <= 0) return false;
+            if (cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+                cudaSuccess)
+                return false;
+            size_t allowance = ((size_t)sm_bytes - (size_t)by_regs * 2048) / (size_t)by_regs;
+            if (allowance > kRingBudget) allowance = kRingBudget;
+            size_t st = allowance / round;
+            if (st > (size_t)kMaxStages) st = kMaxStages;
+            if (st < 2) st = 2;
+            stages = (int)st;
+        }
+        if (occupancy(p->ring ? (size_t)stages * round : 0, &bps) != cudaSuccess || bps <= 0) return false;
+        cached = {stages, bps};
         std::lock_guard<std::mutex> lock(g_mu);
-        g_occupancy[key] = bps;
+        g_plans[key] = cached;
     }
-    int64_t G = (int64_t)sms * bps;
+    p->stages = cached.first;
+    p->smem = p->ring ? (size_t)p->stages * round : 0;
+    int64_t G = (int64_t)sms * cached.second;
     if (G > kMaxCtas) G = kMaxCtas;
     if (G > R) G = R;
     if (G < 1) G = 1;
