@@ -30,7 +30,9 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int TPB = blockDim.x;
-    const int nwarps = TPB >> 5, nquads = (nwarps + 3) >> 2;
+    const int nwarps = TPB >> 5;
+    int ng = 1;  // warps rounded up to a power of two
+    while (ng < nwarps) ng <<= 1;
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t R = a.seg.R, D = a.D, V = D / VE;
     const int64_t r0 = tile_begin(b, R, G), r1 = tile_begin(b + 1, R, G);
@@ -98,12 +100,12 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
     int slot = 0, buf = 0;
     int64_t cur_s = -1;
     bool cur_ok = false;
-    float2 sc1[NV][PV];
-    float2 acc_dy[NV][PV], acc_dyx[NV][PV];
+    f2r sc1[NV][PV];
+    f2r acc_dy[NV][PV], acc_dyx[NV][PV];
 #pragma unroll
     for (int k = 0; k < NV; ++k)
 #pragma unroll
-        for (int p = 0; p < PV; ++p) acc_dy[k][p] = acc_dyx[k][p] = f2(0.0f);
+        for (int p = 0; p < PV; ++p) acc_dy[k][p] = acc_dyx[k][p] = kPairZero;
 
     // Piece (tile b, segment cur_s) done: one fp32 partial row pair in slot b + cur_s.
     auto flush = [&]() {
@@ -114,14 +116,14 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
                 float* pk = P + colb[k] / sizeof(T);  // element offset of my vector k
 #pragma unroll
                 for (int p = 0; p < PV; p += 2) {
-                    *reinterpret_cast<float4*>(pk + 2 * p) =
-                        make_float4(acc_dy[k][p].x, acc_dy[k][p].y, acc_dy[k][p + 1].x, acc_dy[k][p + 1].y);
-                    *reinterpret_cast<float4*>(pk + D + 2 * p) = make_float4(
-                        acc_dyx[k][p].x, acc_dyx[k][p].y, acc_dyx[k][p + 1].x, acc_dyx[k][p + 1].y);
+                    const float2 a0 = p_get(acc_dy[k][p]), a1 = p_get(acc_dy[k][p + 1]);
+                    const float2 b0 = p_get(acc_dyx[k][p]), b1 = p_get(acc_dyx[k][p + 1]);
+                    *reinterpret_cast<float4*>(pk + 2 * p) = make_float4(a0.x, a0.y, a1.x, a1.y);
+                    *reinterpret_cast<float4*>(pk + D + 2 * p) = make_float4(b0.x, b0.y, b1.x, b1.y);
                 }
             }
 #pragma unroll
-            for (int p = 0; p < PV; ++p) acc_dy[k][p] = acc_dyx[k][p] = f2(0.0f);
+            for (int p = 0; p < PV; ++p) acc_dy[k][p] = acc_dyx[k][p] = kPairZero;
         }
     };
 
@@ -170,9 +172,10 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
             for (int k = 0; k < NV; ++k) {
                 uint4 vc = make_uint4(0, 0, 0, 0);
                 if (cur_ok && ok[k]) vc = ld_keep(static_cast<const char*>(a.scale) + m * row_bytes + colb[k]);
-                IO::unpack2(vc, sc1[k]);
+                IO::unpackp(vc, sc1[k]);
+                const f2r one = p_splat(1.0f);
 #pragma unroll
-                for (int p = 0; p < PV; ++p) sc1[k][p] = f2_add(sc1[k][p], f2(1.0f));
+                for (int p = 0; p < PV; ++p) sc1[k][p] = p_add(sc1[k][p], one);
             }
         }
 
@@ -180,31 +183,30 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
             // xhat = (x - mean) * rstd, g = dy * (1 + scale); row sums of g and g*xhat;
             // column sums of dy and dy*xhat. Rows past nr and idle lanes load dy = 0, so they
             // add nothing anywhere.
-            float2 xh[RB][NV][PV], g[RB][NV][PV];
+            f2r xh[RB][NV][PV], g[RB][NV][PV];
             float sums[2 * RB];
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                const float2 rs2 = f2(rs[i]), mu2 = f2(mu[i]);
-                float2 sg[2] = {f2(0.0f), f2(0.0f)}, sgx[2] = {f2(0.0f), f2(0.0f)};
+                const f2r rs2 = p_splat(rs[i]), mu2 = p_splat(mu[i]);
+                f2r sg[2] = {kPairZero, kPairZero}, sgx[2] = {kPairZero, kPairZero};
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
-                    float2 fd[PV];
-                    IO::unpack2(xv[i][k], xh[i][k]);
-                    IO::unpack2(gv[i][k], fd);
+                    f2r fd[PV];
+                    IO::unpackp(xv[i][k], xh[i][k]);
+                    IO::unpackp(gv[i][k], fd);
 #pragma unroll
                     for (int p = 0; p < PV; ++p) {
                         // x - mean first: exact for rows whose mean dwarfs their spread.
-                        xh[i][k][p] = f2_mul(f2_sub(xh[i][k][p], mu2), rs2);
-                        g[i][k][p] = f2_mul(fd[p], sc1[k][p]);
-                        sg[p & 1] = f2_add(sg[p & 1], g[i][k][p]);
-                        sgx[p & 1] = f2_fma(g[i][k][p], xh[i][k][p], sgx[p & 1]);
-                        acc_dy[k][p] = f2_add(acc_dy[k][p], fd[p]);
-                        acc_dyx[k][p] = f2_fma(fd[p], xh[i][k][p], acc_dyx[k][p]);
+                        xh[i][k][p] = p_mul(p_sub(xh[i][k][p], mu2), rs2);
+                        g[i][k][p] = p_mul(fd[p], sc1[k][p]);
+                        sg[p & 1] = p_add(sg[p & 1], g[i][k][p]);
+                        sgx[p & 1] = p_fma(g[i][k][p], xh[i][k][p], sgx[p & 1]);
+                        acc_dy[k][p] = p_add(acc_dy[k][p], fd[p]);
+                        acc_dyx[k][p] = p_fma(fd[p], xh[i][k][p], acc_dyx[k][p]);
                     }
                 }
-                const float2 tg = f2_add(sg[0], sg[1]), tgx = f2_add(sgx[0], sgx[1]);
-                sums[2 * i] = tg.x + tg.y;
-                sums[2 * i + 1] = tgx.x + tgx.y;
+                sums[2 * i] = p_hsum(p_add(sg[0], sg[1]));
+                sums[2 * i + 1] = p_hsum(p_add(sgx[0], sgx[1]));
             }
             warp_sum(sums);
             if (lane == 0) {
@@ -212,22 +214,21 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
                 for (int i = 0; i < 2 * RB; ++i) red[buf][i][warp] = sums[i];
             }
             __syncthreads();
-            cta_sum(red[buf], nquads, sums);
+            cta_sum(red[buf], ng, lane, sums);
             // dx = rstd * (g - mean(g) - xhat * mean(g*xhat))
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 if (i >= nr) continue;
                 const float mg = sums[2 * i] * invD, mgx = sums[2 * i + 1] * invD;
-                const float2 rs2 = f2(rs[i]), nmgx = f2(-mgx), nmgr = f2(-mg * rs[i]);
+                const f2r rs2 = p_splat(rs[i]), nmgx = p_splat(-mgx), nmgr = p_splat(-mg * rs[i]);
                 char* dxr = dxb + (row + i) * row_bytes;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     if (!ok[k]) continue;
-                    float2 o[PV];
+                    f2r o[PV];
 #pragma unroll
-                    for (int p = 0; p < PV; ++p)
-                        o[p] = f2_fma(f2_fma(xh[i][k][p], nmgx, g[i][k][p]), rs2, nmgr);
-                    st_vec(dxr + colb[k], IO::pack2v(o));
+                    for (int p = 0; p < PV; ++p) o[p] = p_fma(p_fma(xh[i][k][p], nmgx, g[i][k][p]), rs2, nmgr);
+                    st_vec(dxr + colb[k], IO::packp(o));
                 }
             }
             buf ^= 1;

@@ -299,6 +299,51 @@ __device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
 }
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
+// The same pair operations on a pair held in one 64-bit register (low half = element 2p,
+// high half = element 2p+1). Keeping pairs in this form end to end lets the compiler feed
+// the f32x2 instructions without repacking 32-bit halves around every operation.
+using f2r = unsigned long long;
+__device__ __forceinline__ f2r p_add(f2r a, f2r b) {
+    f2r d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2r p_sub(f2r a, f2r b) {
+    f2r d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2r p_mul(f2r a, f2r b) {
+    f2r d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2r p_fma(f2r a, f2r b, f2r c) {
+    f2r d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2r p_splat(float v) {
+    f2r d;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(v));
+    return d;
+}
+__device__ __forceinline__ f2r p_make(float lo, float hi) {
+    f2r d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ float2 p_get(f2r a) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(a));
+    return v;
+}
+__device__ __forceinline__ float p_hsum(f2r a) {
+    const float2 v = p_get(a);
+    return v.x + v.y;
+}
+constexpr f2r kPairZero = 0ull;  // (+0.0f, +0.0f)
+
 // ---------------------------------------------------------------------------------------
 // Reductions
 // ---------------------------------------------------------------------------------------
@@ -313,21 +358,17 @@ __device__ __forceinline__ void warp_sum(float (&v)[NVAL]) {
 }
 
 // CTA-wide sum of one value per warp, written by lane 0 of each warp to red[i][warp]; the
-// slots of absent warps (warp >= nwarps) hold zeros. Every thread reads the slots as float4s
-// and adds them in the same fixed order, so all threads of the CTA get the same bits.
+// slots of absent warps hold zeros. ng = the warp count rounded up to a power of two. Every
+// group of ng lanes loads the ng slots and sums them with a butterfly over its own lanes,
+// so each lane ends with the full sum, and all threads of the CTA get the same bits.
 template <int NVAL>
-__device__ __forceinline__ void cta_sum(const float (*red)[32], int nquads, float (&out)[NVAL]) {
+__device__ __forceinline__ void cta_sum(const float (*red)[32], int ng, int lane,
+                                        float (&out)[NVAL]) {
 #pragma unroll
-    for (int i = 0; i < NVAL; ++i) {
-        float t = 0.0f;
+    for (int i = 0; i < NVAL; ++i) out[i] = red[i][lane & (ng - 1)];
+    for (int o = ng >> 1; o >= 1; o >>= 1) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // at most 16 warps a CTA
-            if (q < nquads) {
-                const float4 v = *reinterpret_cast<const float4*>(&red[i][4 * q]);
-                t += (v.x + v.y) + (v.z + v.w);
-            }
-        }
-        out[i] = t;
+        for (int i = 0; i < NVAL; ++i) out[i] += __shfl_xor_sync(0xFFFFFFFFu, out[i], o);
     }
 }
 
@@ -361,6 +402,17 @@ struct Io<float> {
     }
     // Element 0 of a row, from the row's first 32-bit word.
     __device__ static __forceinline__ float first_of_word(uint32_t w) { return __uint_as_float(w); }
+    // As VE/2 pair registers.
+    __device__ static __forceinline__ void unpackp(const uint4& v, f2r* f) {
+        asm("mov.b64 %0, {%1, %2};" : "=l"(f[0]) : "r"(v.x), "r"(v.y));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(f[1]) : "r"(v.z), "r"(v.w));
+    }
+    __device__ static __forceinline__ uint4 packp(const f2r* f) {
+        uint4 v;
+        asm("mov.b64 {%0, %1}, %2;" : "=r"(v.x), "=r"(v.y) : "l"(f[0]));
+        asm("mov.b64 {%0, %1}, %2;" : "=r"(v.z), "=r"(v.w) : "l"(f[1]));
+        return v;
+    }
 };
 
 template <>
@@ -386,6 +438,25 @@ struct Io<__nv_bfloat16> {
         return __uint_as_float(h << 16);
     }
     __device__ static __forceinline__ float first_of_word(uint32_t w) { return __uint_as_float(w << 16); }
+    __device__ static __forceinline__ void unpackp(const uint4& v, f2r* f) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            asm("{\n\t.reg .b32 lo, hi;\n\tshl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xFFFF0000;\n\t"
+                "mov.b64 %0, {lo, hi};\n\t}"
+                : "=l"(f[j])
+                : "r"(w[j]));
+    }
+    // Round each pair to bf16 (nearest, ties to even) and pack it into one 32-bit word.
+    __device__ static __forceinline__ uint4 packp(const f2r* f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+                : "=r"(w[j])
+                : "l"(f[j]));
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
 };
 
 // Streamed (read-once) 16-byte load: read-only path, no L1 allocation.

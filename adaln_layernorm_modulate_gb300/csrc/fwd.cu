@@ -35,7 +35,9 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int TPB = blockDim.x;
-    const int nwarps = TPB >> 5, nquads = (nwarps + 3) >> 2;
+    const int nwarps = TPB >> 5;
+    int ng = 1;  // warps rounded up to a power of two
+    while (ng < nwarps) ng <<= 1;
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t R = a.seg.R, D = a.D, V = D / VE;
     const int64_t r0 = tile_begin(b, R, G), r1 = tile_begin(b + 1, R, G);
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
     int slot = 0;
     int64_t cur_s = -1;
     bool cur_ok = false;
-    float2 sh[NV][PV], sc1[NV][PV];
+    f2r sh[NV][PV], sc1[NV][PV];
     int64_t row, s;
     int nr;
     while (cw.next(a.seg, r1, row, nr, s)) {
@@ -139,33 +141,34 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
                     vs = ld_keep(static_cast<const char*>(a.shift) + m * row_bytes + colb[k]);
                     vc = ld_keep(static_cast<const char*>(a.scale) + m * row_bytes + colb[k]);
                 }
-                IO::unpack2(vs, sh[k]);
-                IO::unpack2(vc, sc1[k]);
+                IO::unpackp(vs, sh[k]);
+                IO::unpackp(vc, sc1[k]);
+                const f2r one = p_splat(1.0f);
 #pragma unroll
-                for (int p = 0; p < PV; ++p) sc1[k][p] = f2_add(sc1[k][p], f2(1.0f));
+                for (int p = 0; p < PV; ++p) sc1[k][p] = p_add(sc1[k][p], one);
             }
         }
 
         if (cur_ok) {  // uniform across the CTA
             // d = x - K, kept for all three passes; idle lanes hold d = 0.
-            float2 d[RB][NV][PV];
+            f2r d[RB][NV][PV];
             float s1[RB];
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                float2 acc0 = f2(0.0f), acc1 = f2(0.0f);
+                const f2r kk = p_splat(K[i]);
+                f2r acc0 = kPairZero, acc1 = kPairZero;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
-                    IO::unpack2(xv[i][k], d[i][k]);
+                    IO::unpackp(xv[i][k], d[i][k]);
 #pragma unroll
                     for (int p = 0; p < PV; ++p) {
-                        d[i][k][p] = f2_sub(d[i][k][p], f2(K[i]));
-                        if (!FULL && !ok[k]) d[i][k][p] = f2(0.0f);
-                        if (p & 1) acc1 = f2_add(acc1, d[i][k][p]);
-                        else acc0 = f2_add(acc0, d[i][k][p]);
+                        d[i][k][p] = p_sub(d[i][k][p], kk);
+                        if (!FULL && !ok[k]) d[i][k][p] = kPairZero;
+                        if (p & 1) acc1 = p_add(acc1, d[i][k][p]);
+                        else acc0 = p_add(acc0, d[i][k][p]);
                     }
                 }
-                const float2 acc = f2_add(acc0, acc1);
-                s1[i] = acc.x + acc.y;
+                s1[i] = p_hsum(p_add(acc0, acc1));
             }
             // Pass 1: mean of d.
             warp_sum(s1);
@@ -174,25 +177,25 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
                 for (int i = 0; i < RB; ++i) red1[i][warp] = s1[i];
             }
             __syncthreads();
-            cta_sum(red1, nquads, s1);
+            cta_sum(red1, ng, lane, s1);
             // Pass 2: centred sum of squares.
             float s2[RB], md[RB];
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 md[i] = s1[i] * invD;
-                float2 acc0 = f2(0.0f), acc1 = f2(0.0f);
+                const f2r pm = p_splat(md[i]);
+                f2r acc0 = kPairZero, acc1 = kPairZero;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
 #pragma unroll
                     for (int p = 0; p < PV; ++p) {
-                        d[i][k][p] = f2_sub(d[i][k][p], f2(md[i]));
-                        if (!FULL && !ok[k]) d[i][k][p] = f2(0.0f);
-                        if (p & 1) acc1 = f2_fma(d[i][k][p], d[i][k][p], acc1);
-                        else acc0 = f2_fma(d[i][k][p], d[i][k][p], acc0);
+                        d[i][k][p] = p_sub(d[i][k][p], pm);
+                        if (!FULL && !ok[k]) d[i][k][p] = kPairZero;
+                        if (p & 1) acc1 = p_fma(d[i][k][p], d[i][k][p], acc1);
+                        else acc0 = p_fma(d[i][k][p], d[i][k][p], acc0);
                     }
                 }
-                const float2 acc = f2_add(acc0, acc1);
-                s2[i] = acc.x + acc.y;
+                s2[i] = p_hsum(p_add(acc0, acc1));
             }
             warp_sum(s2);
             if (lane == 0) {
@@ -200,21 +203,21 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
                 for (int i = 0; i < RB; ++i) red2[i][warp] = s2[i];
             }
             __syncthreads();
-            cta_sum(red2, nquads, s2);
+            cta_sum(red2, ng, lane, s2);
             // Pass 3: y = (d - mean_d) * rstd * (1 + scale) + shift.
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 if (i >= nr) continue;
                 const float rs = rsqrtf(s2[i] * invD + a.eps);
+                const f2r prs = p_splat(rs);
                 char* yr = yb + (row + i) * row_bytes;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
                     if (!ok[k]) continue;
-                    float2 o[PV];
+                    f2r o[PV];
 #pragma unroll
-                    for (int p = 0; p < PV; ++p)
-                        o[p] = f2_fma(f2_mul(d[i][k][p], f2(rs)), sc1[k][p], sh[k][p]);
-                    st_vec(yr + colb[k], IO::pack2v(o));
+                    for (int p = 0; p < PV; ++p) o[p] = p_fma(p_mul(d[i][k][p], prs), sc1[k][p], sh[k][p]);
+                    st_vec(yr + colb[k], IO::packp(o));
                 }
                 if (tid == 0) {
                     a.mean[row + i] = K[i] + md[i];
