@@ -91,13 +91,13 @@ struct Plan {
     int sms;
 };
 
-// One ring round: RB rows of this CTA's vectors of x (and dy for the backward), plus one
-// 4-byte word per thread and per-row scalar (K in the forward, mean and rstd backward).
+// One ring round: RB rows of x (and of dy for the backward), each padded to the CTA's
+// vector grid (nv * tpb * 16 bytes); the ring also holds one mbarrier per slot.
+constexpr size_t kRingHeader = 128;
 size_t ring_round_bytes(Kind kind, const RowCfg& c) {
     const size_t rb = c.nv <= 2 ? 2 : 1;  // RowShape<nv>::kRows
     const size_t row = (size_t)c.tpb * c.nv * 16;
-    const size_t words = (size_t)c.tpb * 4;
-    return kind == kFwd ? rb * (row + words) : rb * (2 * row + 2 * words);
+    return kind == kFwd ? rb * row : rb * 2 * row;
 }
 
 // Launch plan: ring depth from the budget, and row tiles = every resident CTA slot of the
@@ -134,20 +134,21 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
             if (cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
                 cudaSuccess)
                 return false;
-            size_t allowance = ((size_t)sm_bytes - (size_t)by_regs * 2048) / (size_t)by_regs;
+            size_t allowance = ((size_t)sm_bytes - (size_t)by_regs * 2048) / (size_t)by_regs - kRingHeader;
             if (allowance > kRingBudget) allowance = kRingBudget;
             size_t st = allowance / round;
             if (st > (size_t)kMaxStages) st = kMaxStages;
             if (st < 2) st = 2;
             stages = (int)st;
         }
-        if (occupancy(p->ring ? (size_t)stages * round : 0, &bps) != cudaSuccess || bps <= 0) return false;
+        if (occupancy(p->ring ? kRingHeader + (size_t)stages * round : 0, &bps) != cudaSuccess || bps <= 0)
+            return false;
         cached = {stages, bps};
         std::lock_guard<std::mutex> lock(g_mu);
         g_plans[key] = cached;
     }
     p->stages = cached.first;
-    p->smem = p->ring ? (size_t)p->stages * round : 0;
+    p->smem = p->ring ? kRingHeader + (size_t)p->stages * round : 0;
     int64_t G = (int64_t)sms * cached.second;
     if (G > kMaxCtas) G = kMaxCtas;
     if (G > R) G = R;

@@ -11,9 +11,10 @@
 // written as one fp32 partial; stage 2 sums the partials of each modulation row in a
 // fixed order. No float atomics; dy and x are read from HBM exactly once.
 //
-// As in the forward, the ring variant streams each thread's vectors of x and dy (and the
-// rows' saved mean/rstd) `stages - 1` rounds ahead into shared memory with per-thread
-// cp.async, and the elementwise math runs on fp32 pairs.
+// As in the forward, the ring variant has one thread copy whole rows of x and dy into a
+// shared-memory ring with bulk (TMA) copies completing on per-slot mbarriers; the rows'
+// saved mean/rstd are loaded one round ahead into registers; the elementwise math runs on
+// fp32 pairs.
 #include "common.cuh"
 #include "launch.h"
 
@@ -43,20 +44,27 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
     const float invD = 1.0f / (float)D;
     const int ns = a.stages;
 
-    // Ring layout (32-bit shared addresses): [ns][RB][x, dy] rows of NV*TPB vectors, then
-    // [ns][RB][mean, rstd] one word per thread, so the saved statistics arrive with the rows
-    // instead of on the round's critical path.
+    // Ring layout (32-bit shared addresses): ns mbarriers (first 128 bytes), then [ns][RB]
+    // row pairs (x, dy), each row at the offsets it has in global memory.
+    __shared__ int abort_flag;
     const uint32_t vk = (uint32_t)TPB * 16u;
-    const uint32_t vrow = (uint32_t)NV * vk;           // one tensor's row
+    const uint32_t vrow = (uint32_t)NV * vk;           // one tensor's row slot
     const uint32_t vslot = (uint32_t)RB * 2u * vrow;   // one round: RB rows of x and dy
-    const uint32_t ring_sa = smem_addr(ring);
-    const uint32_t my_vec = ring_sa + (uint32_t)tid * 16u;
-    const uint32_t my_st = ring_sa + (uint32_t)ns * vslot + (uint32_t)tid * 4u;
-    const uint32_t strow = (uint32_t)TPB * 8u, stslot = (uint32_t)RB * strow;
+    const uint32_t bars = smem_addr(ring);
+    const uint32_t data = bars + 128u;
+    const uint32_t my_vec = data + (uint32_t)tid * 16u;
 
     zero_absent_warps<2 * RB>(red[0], nwarps);
     zero_absent_warps<2 * RB>(red[1], nwarps);
     uint32_t err = validate_segments<VARLEN>(a.seg, b, G);
+    if constexpr (RING) {
+        if (tid == 0) {
+            for (int q = 0; q < ns; ++q) mbar_init(bars + 8u * q, 1);
+            abort_flag = 0;
+            mbar_fence_init();
+        }
+        __syncthreads();
+    }
 
     uint32_t colb[NV];
     bool ok[NV];
@@ -69,35 +77,44 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
 
     const int64_t s0 = R > 0 ? seg_find<VARLEN>(a.seg, r0) : 0;
     Walker<VARLEN, RB> cw{r0, s0, -1, false};
-    Walker<VARLEN, RB> pw{r0, s0, -1, false};
+    Walker<VARLEN, RB> pw{r0, s0, -1, false};  // producer's walker (thread 0), ns rounds ahead
 
-    auto prefetch = [&](int slot) {
+    // Thread 0: copy the producer walker's next round (x and dy rows) into ring slot `slot`.
+    auto issue = [&](int slot) {
         int64_t rs, sg;
         int nr;
         if (pw.next(a.seg, r1, rs, nr, sg)) {
+            const uint32_t bar = bars + 8u * (uint32_t)slot;
+            mbar_arrive_expect_tx(bar, (uint32_t)(2 * nr * row_bytes));
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 if (i >= nr) continue;
-                const uint32_t xd = my_vec + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
-                const uint32_t st = my_st + (uint32_t)slot * stslot + (uint32_t)i * strow;
+                const uint32_t dst = data + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
                 const int64_t off = (rs + i) * row_bytes;
-                cp_async4_sa(st, a.mean + rs + i);
-                cp_async4_sa(st + (uint32_t)TPB * 4u, a.rstd + rs + i);
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    if (!ok[k]) continue;
-                    cp_async16_sa(xd + (uint32_t)k * vk, xb + off + colb[k]);
-                    cp_async16_sa(xd + vrow + (uint32_t)k * vk, gb + off + colb[k]);
-                }
+                bulk_load(dst, xb + off, (uint32_t)row_bytes, bar);
+                bulk_load(dst + vrow, gb + off, (uint32_t)row_bytes, bar);
             }
         }
-        cp_async_commit();
     };
     if constexpr (RING) {
-        for (int q = 0; q < ns; ++q) prefetch(q);
+        if (tid == 0)
+            for (int q = 0; q < ns; ++q) issue(q);
     }
+    // The saved statistics of the next round's rows, loaded a round ahead (rounds are
+    // consecutive rows of the tile).
+    float mu_n[RB], rs_n[RB];
+    auto load_stats = [&](int64_t first) {
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            const bool in = first + i < r1;
+            mu_n[i] = in ? __ldg(a.mean + first + i) : 0.0f;
+            rs_n[i] = in ? __ldg(a.rstd + first + i) : 0.0f;
+        }
+    };
+    if constexpr (RING) load_stats(r0);
 
     int slot = 0, buf = 0;
+    uint32_t lap = 0;  // completed passes over the ring: the parity of the slot's phase
     int64_t cur_s = -1;
     bool cur_ok = false;
     f2r sc1[NV][PV];
@@ -133,7 +150,13 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
         uint4 xv[RB][NV], gv[RB][NV];
         float mu[RB], rs[RB];
         if constexpr (RING) {
-            cp_async_wait(ns - 1);
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                mu[i] = mu_n[i];
+                rs[i] = rs_n[i];
+            }
+            load_stats(cw.row);
+            if (!mbar_wait_bounded(bars + 8u * (uint32_t)slot, lap & 1u, &abort_flag)) err |= kErrTimeout;
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 const uint32_t xs = my_vec + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
@@ -143,9 +166,6 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
                     xv[i][k] = on ? lds128(xs + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
                     gv[i][k] = on ? lds128(xs + vrow + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
                 }
-                const uint32_t st = my_st + (uint32_t)slot * stslot + (uint32_t)i * strow;
-                mu[i] = i < nr ? __uint_as_float(lds32(st)) : 0.0f;
-                rs[i] = i < nr ? __uint_as_float(lds32(st + (uint32_t)TPB * 4u)) : 0.0f;
             }
         } else {
 #pragma unroll
@@ -214,6 +234,10 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
                 for (int i = 0; i < 2 * RB; ++i) red[buf][i][warp] = sums[i];
             }
             __syncthreads();
+            // Every thread has this slot's rows in registers: refill it ns rounds ahead.
+            if constexpr (RING) {
+                if (tid == 0) issue(slot);
+            }
             cta_sum(red[buf], ng, lane, sums);
             // dx = rstd * (g - mean(g) - xhat * mean(g*xhat))
 #pragma unroll
@@ -234,13 +258,31 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
             buf ^= 1;
         }
         if constexpr (RING) {
-            prefetch(slot);
-            slot = slot + 1 == ns ? 0 : slot + 1;
+            if (!cur_ok) {  // the round was skipped: still wait for every reader, then refill
+                __syncthreads();
+                if (tid == 0) issue(slot);
+            }
+            if (++slot == ns) {
+                slot = 0;
+                ++lap;
+            }
         }
     }
     if (cur_ok) flush();
     if (cw.bad) err |= kErrSeqlens;
-    if constexpr (RING) cp_async_wait_all();
+    if constexpr (RING) {
+        // After a timed-out wait, copies may still be in flight into this CTA's shared
+        // memory: give each slot's outstanding phase one more bounded wait before exiting.
+        __syncthreads();
+        if (tid == 0 && abort_flag) {
+            volatile int never = 0;
+            for (int q = 0; q < ns; ++q) {
+                if (q >= slot && lap == 0) continue;  // never used
+                const uint32_t last = q < slot ? lap : lap - 1;  // pass of the slot's last round
+                mbar_wait_bounded(bars + 8u * q, last & 1u, &never);
+            }
+        }
+    }
     publish_status(err, a.status, a.header);
 }
 

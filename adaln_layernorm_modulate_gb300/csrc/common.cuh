@@ -27,7 +27,7 @@ constexpr size_t kStatusWordsBytes = sizeof(uint32_t) * kMaxCtas;
 constexpr size_t kPartialsOffset = kHeaderBytes + kStatusWordsBytes;
 constexpr uint32_t kStatusMagic = 0x4E4C4441u;  // "ADLN"
 
-enum : uint32_t { kErrSeqlens = 1u, kErrModIdx = 2u };
+enum : uint32_t { kErrSeqlens = 1u, kErrModIdx = 2u, kErrTimeout = 4u };
 
 struct WsHeader {
     uint32_t magic;
@@ -152,6 +152,7 @@ __device__ __forceinline__ void publish_status(uint32_t err, uint32_t* words, Ws
     uint32_t all = 0;
     if (__syncthreads_or((int)(err & kErrSeqlens))) all |= kErrSeqlens;
     if (__syncthreads_or((int)(err & kErrModIdx))) all |= kErrModIdx;
+    if (__syncthreads_or((int)(err & kErrTimeout))) all |= kErrTimeout;
     if (words == nullptr || threadIdx.x != 0) return;
     words[blockIdx.x] = all;
     if (blockIdx.x == 0) {
@@ -242,6 +243,65 @@ __device__ __forceinline__ void cp_async_wait(int n) {
     }
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------
+// Bulk (TMA) row copies into a shared-memory ring, completed on an mbarrier per slot.
+// One thread issues a whole row with one instruction; every thread waits on the slot's
+// mbarrier. Every wait is bounded: after kWaitLimitNs it sets the CTA's abort flag (so no
+// later wait lingers), reports failure, and the kernel carries on with whatever is in the
+// slot, so a stuck copy can cost at most one bounded wait, never a hang.
+// ---------------------------------------------------------------------------------------
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// Makes initialised mbarriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// One contiguous global -> shared copy of `bytes` (a multiple of 16, both ends 16-byte
+// aligned) that completes `bytes` of the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for phase `parity` of the mbarrier; false (and *abort set) if it did not complete
+// within kWaitLimitNs, or immediately if another thread already gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (*abort) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
 
 // Lets `fn` use, with its static shared memory, up to the device's opt-in shared memory per
 // block (host side).

@@ -7,12 +7,12 @@
 // in registers and the three passes (sum, centred sum of squares, modulated write) run
 // over registers, touching HBM once for x and once for y.
 //
-// Memory-level parallelism: in the ring variant every thread streams its own vectors of
-// the next `stages - 1` rounds into shared memory with cp.async while it works on the
-// current round (each thread reads back only what it copied, so the ring needs no
-// cross-thread synchronisation). The plain variant, used when a row is too wide for a
-// ring of two rounds, loads straight into registers. FULL: the CTA's threads cover the
-// row exactly (no idle vector slots), so no lane masking is needed.
+// Memory-level parallelism: in the ring variant one thread copies whole rows into a
+// shared-memory ring of `stages` rounds with bulk (TMA) copies, one instruction per row,
+// completing on a per-slot mbarrier; it refills a slot as soon as the CTA's first barrier
+// of the round shows every thread has read it. The plain variant, used when a row is too
+// wide for a ring of two rounds, loads straight into registers. FULL: the CTA's threads
+// cover the row exactly (no idle vector slots), so no lane masking is needed.
 //
 // Variance: sum and centred sum of squares of d = x - x[row, 0]. Subtracting the row's
 // first element first (shifted data, Chan, Golub & LeVeque 1983) keeps the fp32 sums of
@@ -47,20 +47,28 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
     const float invD = 1.0f / (float)D;
     const int ns = a.stages;
 
-    // Ring layout (32-bit shared addresses): [ns][RB] rows of NV*TPB vectors, then [ns][RB]
-    // words of each row's element 0, one per thread (the row's shift point K, read without
-    // cross-thread synchronisation).
-    const uint32_t vk = (uint32_t)TPB * 16u;             // one vector index k across the CTA
-    const uint32_t vrow = (uint32_t)NV * vk;           // one row
+    // Ring layout (32-bit shared addresses): ns mbarriers (first 128 bytes), then [ns][RB]
+    // rows, each row at the offsets it has in global memory (thread t's vector k at
+    // (t + k*TPB)*16), so a bulk copy lands every thread's vectors where it reads them.
+    __shared__ int abort_flag;
+    const uint32_t vk = (uint32_t)TPB * 16u;           // one vector index k across the CTA
+    const uint32_t vrow = (uint32_t)NV * vk;           // one row slot
     const uint32_t vslot = (uint32_t)RB * vrow;        // one round
-    const uint32_t ring_sa = smem_addr(ring);
-    const uint32_t my_vec = ring_sa + (uint32_t)tid * 16u;
-    const uint32_t my_k = ring_sa + (uint32_t)ns * vslot + (uint32_t)tid * 4u;
-    const uint32_t krow = (uint32_t)TPB * 4u, kslot = (uint32_t)RB * krow;
+    const uint32_t bars = smem_addr(ring);
+    const uint32_t data = bars + 128u;
+    const uint32_t my_vec = data + (uint32_t)tid * 16u;
 
     zero_absent_warps<RB>(red1, nwarps);
     zero_absent_warps<RB>(red2, nwarps);
     uint32_t err = validate_segments<VARLEN>(a.seg, b, G);
+    if constexpr (RING) {
+        if (tid == 0) {
+            for (int q = 0; q < ns; ++q) mbar_init(bars + 8u * q, 1);
+            abort_flag = 0;
+            mbar_fence_init();
+        }
+        __syncthreads();
+    }
 
     uint32_t colb[NV];  // byte offset of my vector k within a row
     bool ok[NV];
@@ -73,31 +81,29 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
 
     const int64_t s0 = R > 0 ? seg_find<VARLEN>(a.seg, r0) : 0;
     Walker<VARLEN, RB> cw{r0, s0, -1, false};
-    Walker<VARLEN, RB> pw{r0, s0, -1, false};
+    Walker<VARLEN, RB> pw{r0, s0, -1, false};  // producer's walker (thread 0), ns rounds ahead
 
-    // Copy this thread's vectors of the prefetch walker's next round into ring slot `slot`.
-    auto prefetch = [&](int slot) {
+    // Thread 0: copy the producer walker's next round into ring slot `slot`.
+    auto issue = [&](int slot) {
         int64_t rs, sg;
         int nr;
         if (pw.next(a.seg, r1, rs, nr, sg)) {
+            const uint32_t bar = bars + 8u * (uint32_t)slot;
+            mbar_arrive_expect_tx(bar, (uint32_t)(nr * row_bytes));
 #pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                if (i >= nr) continue;
-                const char* src = xb + (rs + i) * row_bytes;
-                const uint32_t dst = my_vec + (uint32_t)slot * vslot + (uint32_t)i * vrow;
-                cp_async4_sa(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow, src);
-#pragma unroll
-                for (int k = 0; k < NV; ++k)
-                    if (ok[k]) cp_async16_sa(dst + (uint32_t)k * vk, src + colb[k]);
-            }
+            for (int i = 0; i < RB; ++i)
+                if (i < nr)
+                    bulk_load(data + (uint32_t)slot * vslot + (uint32_t)i * vrow, xb + (rs + i) * row_bytes,
+                              (uint32_t)row_bytes, bar);
         }
-        cp_async_commit();
     };
     if constexpr (RING) {
-        for (int q = 0; q < ns; ++q) prefetch(q);
+        if (tid == 0)
+            for (int q = 0; q < ns; ++q) issue(q);
     }
 
     int slot = 0;
+    uint32_t lap = 0;  // completed passes over the ring: the parity of the slot's phase
     int64_t cur_s = -1;
     bool cur_ok = false;
     f2r sh[NV][PV], sc1[NV][PV];
@@ -107,15 +113,14 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
         uint4 xv[RB][NV];
         float K[RB];
         if constexpr (RING) {
-            cp_async_wait(ns - 1);
+            if (!mbar_wait_bounded(bars + 8u * (uint32_t)slot, lap & 1u, &abort_flag)) err |= kErrTimeout;
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                const uint32_t src = my_vec + (uint32_t)slot * vslot + (uint32_t)i * vrow;
+                const uint32_t rowsa = (uint32_t)slot * vslot + (uint32_t)i * vrow;
 #pragma unroll
                 for (int k = 0; k < NV; ++k)
-                    xv[i][k] = (i < nr && ok[k]) ? lds128(src + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
-                K[i] = (i < nr) ? IO::first_of_word(lds32(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow))
-                                : 0.0f;
+                    xv[i][k] = (i < nr && ok[k]) ? lds128(my_vec + rowsa + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                K[i] = (i < nr) ? IO::first_of_word(lds32(data + rowsa)) : 0.0f;
             }
         } else {
 #pragma unroll
@@ -177,6 +182,10 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
                 for (int i = 0; i < RB; ++i) red1[i][warp] = s1[i];
             }
             __syncthreads();
+            // Every thread has this slot's rows in registers: refill it ns rounds ahead.
+            if constexpr (RING) {
+                if (tid == 0) issue(slot);
+            }
             cta_sum(red1, ng, lane, s1);
             // Pass 2: centred sum of squares.
             float s2[RB], md[RB];
@@ -226,12 +235,30 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
             }
         }
         if constexpr (RING) {
-            prefetch(slot);  // this slot's data is in registers: refill it `ns` rounds ahead
-            slot = slot + 1 == ns ? 0 : slot + 1;
+            if (!cur_ok) {  // the round was skipped: still wait for every reader, then refill
+                __syncthreads();
+                if (tid == 0) issue(slot);
+            }
+            if (++slot == ns) {
+                slot = 0;
+                ++lap;
+            }
         }
     }
     if (cw.bad) err |= kErrSeqlens;
-    if constexpr (RING) cp_async_wait_all();
+    if constexpr (RING) {
+        // After a timed-out wait, copies may still be in flight into this CTA's shared
+        // memory: give each slot's outstanding phase one more bounded wait before exiting.
+        __syncthreads();
+        if (tid == 0 && abort_flag) {
+            volatile int never = 0;
+            for (int q = 0; q < ns; ++q) {
+                if (q >= slot && lap == 0) continue;  // never used
+                const uint32_t last = q < slot ? lap : lap - 1;  // pass of the slot's last round
+                mbar_wait_bounded(bars + 8u * q, last & 1u, &never);
+            }
+        }
+    }
     publish_status(err, a.status, a.header);
 }
 
