@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
 
     int slot = 0, buf = 0;
     uint32_t lap = 0;  // completed passes over the ring: the parity of the slot's phase
+    bool started = false;  // a previous round exists whose slot can be refilled
     int64_t cur_s = -1;
     bool cur_ok = false;
     f2r sc1[NV][PV];
@@ -156,6 +157,10 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
                 rs[i] = rs_n[i];
             }
             load_stats(cw.row);
+            // The previous round's slot has been read by every thread (they all passed that
+            // round's barriers): refill it ns rounds ahead before waiting on this one.
+            if (tid == 0 && started) issue(slot == 0 ? ns - 1 : slot - 1);
+            started = true;
             if (!mbar_wait_bounded(bars + 8u * (uint32_t)slot, lap & 1u, &abort_flag)) err |= kErrTimeout;
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
@@ -234,10 +239,6 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
                 for (int i = 0; i < 2 * RB; ++i) red[buf][i][warp] = sums[i];
             }
             __syncthreads();
-            // Every thread has this slot's rows in registers: refill it ns rounds ahead.
-            if constexpr (RING) {
-                if (tid == 0) issue(slot);
-            }
             cta_sum(red[buf], ng, lane, sums);
             // dx = rstd * (g - mean(g) - xhat * mean(g*xhat))
 #pragma unroll
@@ -258,10 +259,7 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
             buf ^= 1;
         }
         if constexpr (RING) {
-            if (!cur_ok) {  // the round was skipped: still wait for every reader, then refill
-                __syncthreads();
-                if (tid == 0) issue(slot);
-            }
+            if (!cur_ok) __syncthreads();  // a skipped round still fences the slot's readers
             if (++slot == ns) {
                 slot = 0;
                 ++lap;
