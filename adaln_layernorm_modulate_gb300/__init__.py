@@ -24,7 +24,7 @@ ADALN_F32, ADALN_BF16 = 0, 1
 STATUS = {
     0: "ADALN_OK", 1: "ADALN_ERR_INVALID_ARG", 2: "ADALN_ERR_UNSUPPORTED",
     3: "ADALN_ERR_ALIGNMENT", 4: "ADALN_ERR_WORKSPACE", 5: "ADALN_ERR_CUDA",
-    6: "ADALN_ERR_BAD_SEQLENS", 7: "ADALN_ERR_BAD_MOD_IDX",
+    6: "ADALN_ERR_BAD_SEQLENS", 7: "ADALN_ERR_BAD_MOD_IDX", 8: "ADALN_ERR_TIMEOUT",
 }
 EXPORTS = (
     "adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd", "adaln_bwd_partials", "adaln_bwd_reduce",

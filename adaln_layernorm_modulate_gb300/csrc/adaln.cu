@@ -95,9 +95,9 @@ struct Plan {
 // vector grid (nv * tpb * 16 bytes); the ring also holds one mbarrier per slot.
 constexpr size_t kRingHeader = 128;
 size_t ring_round_bytes(Kind kind, const RowCfg& c) {
-    const size_t rb = c.nv <= 2 ? 2 : 1;  // RowShape<nv>::kRows
     const size_t row = (size_t)c.tpb * c.nv * 16;
-    return kind == kFwd ? rb * row : rb * 2 * row;
+    if (kind == kFwd) return (c.nv <= 3 ? 2 : 1) * row;  // RowShape<nv>::kFwdRows
+    return (c.nv <= 2 ? 2 : 1) * 2 * row;                // RowShape<nv>::kRows, x and dy
 }
 
 // Launch plan: ring depth from the budget, and row tiles = every resident CTA slot of the
@@ -468,6 +468,7 @@ int adaln_read_status(const void* workspace, cudaStream_t stream) {
     for (uint32_t w : words) all |= w;
     if (all & kErrSeqlens) return ADALN_ERR_BAD_SEQLENS;
     if (all & kErrModIdx) return ADALN_ERR_BAD_MOD_IDX;
+    if (all & kErrTimeout) return ADALN_ERR_TIMEOUT;
     return ADALN_OK;
 }
 
@@ -492,6 +493,7 @@ const char* adaln_status_string(int status) {
         case ADALN_ERR_CUDA: return "ADALN_ERR_CUDA: CUDA runtime error";
         case ADALN_ERR_BAD_SEQLENS: return "ADALN_ERR_BAD_SEQLENS: malformed cu_seqlens";
         case ADALN_ERR_BAD_MOD_IDX: return "ADALN_ERR_BAD_MOD_IDX: mod_idx out of range";
+        case ADALN_ERR_TIMEOUT: return "ADALN_ERR_TIMEOUT: a kernel timed out waiting for its input copies";
         default: return "unknown adaln status";
     }
 }

@@ -285,14 +285,25 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const Bw
 }
 
 // Stage 2: dshift[m] / dscale[m] = sum of the partials of every piece of every segment
-// whose modulation row is m, in a fixed order. CTA (blockIdx.x, m) covers `cw` float4
-// columns; its 256 threads form cw columns x (256 / cw) splits of m's piece list (piece j
-// goes to split j mod splits), combined by a fixed shared-memory tree.
+// whose modulation row is m, in a fixed order. The pieces of m form a flat list in segment
+// order (piece = tile b of segment s, partial slot b + s). CTA (blockIdx.x, m) covers `cw`
+// float4 columns; its 256 threads form cw columns x (256 / cw) splits, piece j going to
+// split j mod splits; each split adds its pieces in list order (kStage2Unroll loads in
+// flight at a time), and a fixed shared-memory tree combines the splits.
+//
+// Packed batches find m's segments by compacting the segment table a chunk at a time:
+// every thread tests kStage2Per consecutive entries, and one block-wide scan places the
+// hits, in order, with the flat index of their first piece.
+constexpr int kStage2Per = 4;
+constexpr int kStage2Chunk = kStage2Threads * kStage2Per;
+constexpr int kStage2Unroll = 4;
+
 template <bool VARLEN>
-__global__ void __launch_bounds__(kStage2Threads) stage2_kernel(const Stage2Args a) {
+__global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2Args a) {
     __shared__ float4 red[2][kStage2Threads];
-    __shared__ int32_t list[kStage2Threads];
-    __shared__ int32_t warp_count[kStage2Threads / 32];
+    __shared__ uint32_t hit_slot[kStage2Chunk];       // partial slot of the hit's first piece
+    __shared__ int32_t hit_first[kStage2Chunk + 1];   // flat index of the hit's first piece
+    __shared__ int32_t warp_tot[2][kStage2Threads / 32];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cw = a.cw, splits = kStage2Threads / cw;
@@ -301,49 +312,122 @@ __global__ void __launch_bounds__(kStage2Threads) stage2_kernel(const Stage2Args
     const int64_t c4 = (int64_t)blockIdx.x * cw + ci;
     const bool cok = c4 < D4;
     const int64_t R = a.seg.R, G = a.G;
-    const float4* P = reinterpret_cast<const float4*>(a.partials);
+    const float4* P = reinterpret_cast<const float4*>(a.partials) + c4;
 
     for (int64_t m = blockIdx.y; m < a.seg.nmod; m += gridDim.y) {
         float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-        int64_t J = 0;  // pieces of row m seen so far, in segment order
+        int64_t J = 0;  // pieces of row m before the current list
 
-        auto add_segment = [&](int64_t s) {
-            const int64_t lo = max((int64_t)0, min(seg_start<VARLEN>(a.seg, s), R));
-            const int64_t hi = max((int64_t)0, min(seg_start<VARLEN>(a.seg, s + 1), R));
-            if (hi <= lo) return;
-            const int64_t blo = tile_of_row(lo, R, G), bhi = tile_of_row(hi - 1, R, G);
-            const int64_t n = bhi - blo + 1;
-            for (int64_t j = ((k - J) % splits + splits) % splits; j < n; j += splits) {
-                const int64_t slot = blo + j + s;
-                if (cok) {
-                    const float4 u = P[(slot * 2 + 0) * D4 + c4];
-                    const float4 v = P[(slot * 2 + 1) * D4 + c4];
-                    acc0.x += u.x; acc0.y += u.y; acc0.z += u.z; acc0.w += u.w;
-                    acc1.x += v.x; acc1.y += v.y; acc1.z += v.z; acc1.w += v.w;
+        // Add this thread's share of pieces [0, n) of the current list (global index J + q),
+        // piece q sitting in partial slot slot_of(q).
+        auto sum_pieces = [&](int64_t n, auto slot_of) {
+            if (cok) {
+                for (int64_t q0 = (int64_t)((k - J) & (int64_t)(splits - 1)); q0 < n;
+                     q0 += (int64_t)kStage2Unroll * splits) {
+                    float4 u[kStage2Unroll], v[kStage2Unroll];
+#pragma unroll
+                    for (int i = 0; i < kStage2Unroll; ++i) {
+                        const int64_t q = q0 + (int64_t)i * splits;
+                        if (q < n) {
+                            const int64_t slot = slot_of(q);
+                            u[i] = __ldg(P + (slot * 2 + 0) * D4);
+                            v[i] = __ldg(P + (slot * 2 + 1) * D4);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kStage2Unroll; ++i) {
+                        if (q0 + (int64_t)i * splits < n) {
+                            acc0.x += u[i].x; acc0.y += u[i].y; acc0.z += u[i].z; acc0.w += u[i].w;
+                            acc1.x += v[i].x; acc1.y += v[i].y; acc1.z += v[i].z; acc1.w += v[i].w;
+                        }
+                    }
                 }
             }
             J += n;
         };
 
         if constexpr (!VARLEN) {
-            add_segment(m);
+            const int64_t lo = min(m * a.seg.N, R), hi = min((m + 1) * a.seg.N, R);
+            if (hi > lo) {
+                const int64_t blo = tile_of_row(lo, R, G), bhi = tile_of_row(hi - 1, R, G);
+                sum_pieces(bhi - blo + 1, [&](int64_t q) { return blo + q + m; });
+            }
         } else {
-            // Ordered scan of the segment table for the segments that use row m.
-            for (int64_t base = 0; base < a.seg.nseg; base += kStage2Threads) {
-                const int64_t s = base + tid;
-                const bool hit = s < a.seg.nseg && (int64_t)__ldg(a.seg.mod + s) == m;
-                const unsigned mask = __ballot_sync(0xFFFFFFFFu, hit);
-                if (lane == 0) warp_count[warp] = __popc(mask);
-                __syncthreads();
-                int offset = 0, total = 0;
-                for (int w = 0; w < kStage2Threads / 32; ++w) {
-                    if (w < warp) offset += warp_count[w];
-                    total += warp_count[w];
+            for (int64_t base = 0; base < a.seg.nseg; base += kStage2Chunk) {
+                // This thread's entries: segments s0 .. s0 + kStage2Per - 1 of the chunk.
+                const int64_t s0 = base + (int64_t)tid * kStage2Per;
+                int32_t np[kStage2Per];
+                uint32_t sl[kStage2Per];
+                int hc = 0, pc = 0;
+#pragma unroll
+                for (int i = 0; i < kStage2Per; ++i) {
+                    const int64_t s = s0 + i;
+                    np[i] = 0;
+                    sl[i] = 0;
+                    if (s < a.seg.nseg && (int64_t)__ldg(a.seg.mod + s) == m) {
+                        // Clamp into [0, R] so a malformed table cannot index past the slots.
+                        const int64_t lo = max((int64_t)0, min(seg_start<true>(a.seg, s), R));
+                        const int64_t hi = max((int64_t)0, min(seg_start<true>(a.seg, s + 1), R));
+                        if (hi > lo) {
+                            const int64_t blo = tile_of_row(lo, R, G), bhi = tile_of_row(hi - 1, R, G);
+                            np[i] = (int32_t)(bhi - blo + 1);
+                            sl[i] = (uint32_t)(blo + s);
+                            ++hc;
+                            pc += np[i];
+                        }
+                    }
                 }
-                if (hit) list[offset + __popc(mask & ((1u << lane) - 1u))] = (int32_t)s;
+                // Block-wide exclusive scan of (hits, pieces) in thread order = table order.
+                int ih = hc, ip = pc;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int th = __shfl_up_sync(0xFFFFFFFFu, ih, o);
+                    const int tp = __shfl_up_sync(0xFFFFFFFFu, ip, o);
+                    if (lane >= o) {
+                        ih += th;
+                        ip += tp;
+                    }
+                }
+                if (lane == 31) {
+                    warp_tot[0][warp] = ih;
+                    warp_tot[1][warp] = ip;
+                }
                 __syncthreads();
-                for (int i = 0; i < total; ++i) add_segment(list[i]);
+                int oh = ih - hc, op = ip - pc, H = 0, NP = 0;
+#pragma unroll
+                for (int w = 0; w < kStage2Threads / 32; ++w) {
+                    const int th = warp_tot[0][w], tp = warp_tot[1][w];
+                    if (w < warp) {
+                        oh += th;
+                        op += tp;
+                    }
+                    H += th;
+                    NP += tp;
+                }
+#pragma unroll
+                for (int i = 0; i < kStage2Per; ++i) {
+                    if (np[i] > 0) {
+                        hit_slot[oh] = sl[i];
+                        hit_first[oh] = op;
+                        ++oh;
+                        op += np[i];
+                    }
+                }
+                if (tid == 0) hit_first[H] = NP;
                 __syncthreads();
+                if (H > 0) {
+                    sum_pieces(NP, [&](int64_t q) {
+                        // The hit holding piece q: the last h with hit_first[h] <= q.
+                        int lo = 0, hi = H - 1;
+                        while (lo < hi) {
+                            const int mid = (lo + hi + 1) >> 1;
+                            if ((int64_t)hit_first[mid] <= q) lo = mid;
+                            else hi = mid - 1;
+                        }
+                        return (int64_t)hit_slot[lo] + (q - (int64_t)hit_first[lo]);
+                    });
+                }
+                __syncthreads();  // the next chunk reuses the hit lists and warp totals
             }
         }
 

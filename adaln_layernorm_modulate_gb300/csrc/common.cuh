@@ -18,6 +18,9 @@ constexpr int kMaxStages = 8;       // deepest shared-memory ring, in rounds
 template <int NV>
 struct RowShape {
     static constexpr int kRows = NV <= 2 ? 2 : 1;
+    // The forward holds one row's values where the backward holds two (x and dy), so it
+    // can take two rows a round up to NV = 3.
+    static constexpr int kFwdRows = NV <= 3 ? 2 : 1;
     static constexpr int kMaxThreads = NV == 1 || NV >= 8 ? 512 : 384;
 };
 

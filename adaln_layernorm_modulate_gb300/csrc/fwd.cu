@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
     using IO = Io<T>;
     constexpr int VE = IO::VE;
     constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector
-    constexpr int RB = RowShape<NV>::kRows;
+    constexpr int RB = RowShape<NV>::kFwdRows;
     extern __shared__ uint4 ring[];
     __shared__ __align__(16) float red1[RB][32];
     __shared__ __align__(16) float red2[RB][32];

@@ -75,7 +75,10 @@ typedef enum {
     ADALN_ERR_WORKSPACE = 4,    /* workspace null or smaller than required              */
     ADALN_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed          */
     ADALN_ERR_BAD_SEQLENS = 6,  /* device data: cu_seqlens malformed (adaln_read_status) */
-    ADALN_ERR_BAD_MOD_IDX = 7   /* device data: mod_idx out of range (adaln_read_status) */
+    ADALN_ERR_BAD_MOD_IDX = 7,  /* device data: mod_idx out of range (adaln_read_status) */
+    ADALN_ERR_TIMEOUT = 8       /* a kernel gave up waiting (1 s) for a bulk copy of its
+                                   input rows; the rows it had not finished are unwritten
+                                   (adaln_read_status) */
 } adaln_status;
 
 /* Forward, dense batch x[Bt, N, D]; token (b, n) uses shift[b], scale[b].
@@ -148,10 +151,13 @@ int adaln_bwd_varlen_reduce(const void* dy, const void* x, const float* mean, co
                             int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
                             size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream);
 
-/* Synchronises `stream`, then returns the device-side data status recorded in `workspace`
- * by the last packed forward/backward (or backward) that used it: ADALN_OK,
- * ADALN_ERR_BAD_SEQLENS or ADALN_ERR_BAD_MOD_IDX (ADALN_ERR_CUDA if the copy fails,
- * ADALN_ERR_WORKSPACE if the workspace holds no status). */
+/* Synchronises `stream`, then returns the device-side status recorded in `workspace` by
+ * the last packed forward/backward (or backward) that used it: ADALN_OK,
+ * ADALN_ERR_BAD_SEQLENS, ADALN_ERR_BAD_MOD_IDX or ADALN_ERR_TIMEOUT, in that order of
+ * precedence (ADALN_ERR_CUDA if the copy fails, ADALN_ERR_WORKSPACE if the workspace holds
+ * no status). Every wait a kernel makes on its own bulk copies is bounded (1 s); a kernel
+ * that runs out of time stops, drains the copies it started and records the timeout. The
+ * dense forward takes no workspace, so it has nowhere to record one. */
 int adaln_read_status(const void* workspace, cudaStream_t stream);
 
 /* Bytes of the fixed scratch array adaln_bwd_noalloc uses on every device that loads the

@@ -170,6 +170,17 @@ BUCKET_P = 2
 MMDIT_TEXT_N, MMDIT_VIDEO_N = 512, 32760
 
 
+def bucket(S: int, bucket_batch: Callable[[int, int, int, int], int], generate: bool = True) -> Workload:
+    """One bucket of workload 3 as its own packed call: bucket_batch(S, ...) segments of
+    length S, bf16, D=3072, one modulation row per segment, x and dy as workload 1."""
+    B = int(bucket_batch(S, BUCKET_M_MEM, BUCKET_M_COMP, BUCKET_P))
+    w = make("bucket-s%d-bf16-d3072-%dseg" % (S, B), 3, BF16, 3072, [S] * B,
+             x_mode=ROWS_SCALED, mod_std=0.1, dy_std=0.02, generate=generate)
+    w.meta["batches"] = [B]
+    w.meta["bucket_s"] = [S]
+    return w
+
+
 def config(idx: int, bucket_batch: Optional[Callable[[int, int, int, int], int]] = None,
            dtype: Optional[int] = None, generate: bool = True) -> Workload:
     """Build workload `idx` (0..4).
@@ -200,6 +211,7 @@ def config(idx: int, bucket_batch: Optional[Callable[[int, int, int, int], int]]
         w = make("varlen-bf16-d3072-%dseg" % len(lens), 3, BF16, 3072, lens,
                  x_mode=ROWS_SCALED, mod_std=0.1, dy_std=0.02, generate=generate)
         w.meta["batches"] = batches
+        w.meta["bucket_s"] = list(BUCKET_S)
         return w
     if idx == 4:
         dt = F32 if dtype is None else dtype

@@ -98,6 +98,17 @@ SMALL = {
         "c", 111, synth.F32, 128, list(np.random.default_rng(5).integers(0, 10, 100)),
         list(np.random.default_rng(6).integers(0, 13, 100)), 13),
     "dense-f32-one-row": lambda: synth.dense("c", 112, synth.F32, 1, 1, 1536),
+    # More segments than stage 2 examines in one pass of the table (1024), rows of the
+    # modulation table whose segments fall in several passes, and empty segments.
+    "packed-f32-d64-3000seg": lambda: synth.make(
+        "c", 113, synth.F32, 64, list(np.random.default_rng(7).integers(0, 10, 3000)),
+        list(np.random.default_rng(8).integers(0, 40, 3000)), 41),
+    # One long segment spread over many row tiles, sharing its modulation row with
+    # thousands of short ones.
+    "packed-bf16-d256-long-and-many": lambda: synth.make(
+        "c", 114, synth.BF16, 256, [5000] + list(np.random.default_rng(9).integers(1, 8, 2500)),
+        [0] + list(np.random.default_rng(10).integers(0, 3, 2500)), 3,
+        x_mode=synth.ROWS_SCALED, dy_std=0.02),
 }
 
 
@@ -251,6 +262,28 @@ def test_malformed_tables_report_status_without_faulting():
     _, mean, rstd, st = H.gpu_fwd(d)
     assert st == 0
     assert H.gpu_bwd(d, mean, rstd)[3] == 0
+
+
+def test_status_words_decode_with_precedence():
+    """adaln_read_status on workspace words written from the host: the per-CTA bits a
+    kernel can record (1 cu_seqlens, 2 mod_idx, 4 copy timeout) map to their status, the
+    table errors first; a header without the magic reads as a missing status."""
+    import adaln_layernorm_modulate_gb300 as A
+    t = H.torch()
+
+    def status(words, magic=0x4E4C4441):
+        head = np.zeros(64, dtype=np.uint32)  # 256-byte header: magic, word count, padding
+        head[0], head[1] = magic, len(words)
+        buf = np.concatenate([head, np.asarray(words, dtype=np.uint32)])
+        ws = t.from_numpy(buf.view(np.uint8)).cuda()
+        return A.STATUS[A.adaln_read_status(ws)]
+
+    assert status([0, 0, 0]) == "ADALN_OK"
+    assert status([0, 4, 0]) == "ADALN_ERR_TIMEOUT"
+    assert status([4, 2, 0]) == "ADALN_ERR_BAD_MOD_IDX"
+    assert status([4, 2, 1]) == "ADALN_ERR_BAD_SEQLENS"
+    assert status([0, 4], magic=0) == "ADALN_ERR_WORKSPACE"
+    assert status([]) == "ADALN_ERR_WORKSPACE"
 
 
 def test_empty_and_zero_length_segments(orc):
