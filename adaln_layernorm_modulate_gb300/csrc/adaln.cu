@@ -77,13 +77,16 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
 
 enum Kind { kFwd = 0, kBwd = 1 };
 
-// Most shared memory a CTA gives its cp.async ring (two such CTAs fit on one SM); less when
+// Most shared memory a CTA gives its ring (two such CTAs fit on one SM); less when
 // registers let more CTAs share the SM.
 constexpr size_t kRingBudget = 100 * 1024;
+// Forward tiles at least this many rows long stage rows with the per-thread copy ring,
+// shorter ones with the bulk ring (which starts faster, see fwd.cu).
+constexpr int64_t kCopyRingRows = 256;
 
 struct Plan {
     RowCfg c;
-    bool ring;      // cp.async shared-memory ring (false: plain loads into registers)
+    int ring;       // kRingNone (plain loads into registers), kRingBulk or kRingCopy
     bool full;      // ring kernel specialised for rows the CTA covers exactly
     int stages;     // ring depth in rounds
     size_t smem;    // dynamic shared memory per CTA
@@ -92,27 +95,21 @@ struct Plan {
 };
 
 // One ring round: RB rows of x (and of dy for the backward), each padded to the CTA's
-// vector grid (nv * tpb * 16 bytes); the ring also holds one mbarrier per slot.
+// vector grid (nv * tpb * 16 bytes), plus for the copy ring one word per thread and row
+// (its copy of the row's first element). The ring also holds one mbarrier per slot.
 constexpr size_t kRingHeader = 128;
-size_t ring_round_bytes(Kind kind, const RowCfg& c) {
+size_t ring_round_bytes(Kind kind, const RowCfg& c, int ring) {
     const size_t row = (size_t)c.tpb * c.nv * 16;
-    if (kind == kFwd) return (c.nv <= 3 ? 2 : 1) * row;  // RowShape<nv>::kFwdRows
-    return (c.nv <= 2 ? 2 : 1) * 2 * row;                // RowShape<nv>::kRows, x and dy
+    if (kind == kFwd)  // RowShape<nv>::kFwdRows rows
+        return (c.nv <= 3 ? 2 : 1) * (ring == kRingCopy ? row + (size_t)c.tpb * 4 : row);
+    return (c.nv <= 2 ? 2 : 1) * 2 * row;  // RowShape<nv>::kRows, x and dy
 }
 
-// Launch plan: ring depth from the budget, and row tiles = every resident CTA slot of the
-// device (at most one per row).
-bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, Plan* p) {
-    int dev = 0;
-    const int sms = current_sms(&dev);
-    if (sms <= 0) return false;
-    p->sms = sms;
-    p->c = row_cfg(D, dtype, kind == kFwd);
-    const size_t round = ring_round_bytes(kind, p->c);
-    p->ring = kRingBudget / round >= 2;
-    p->full = p->ring && p->c.full;
+// Ring depth and resident CTAs per SM of one kernel variant (cached per device).
+bool ring_shape(Kind kind, adaln_dtype dtype, bool varlen, int dev, Plan* p) {
+    const size_t round = p->ring ? ring_round_bytes(kind, p->c, p->ring) : 0;
     const auto key = std::make_tuple(dev, (int)kind, (int)dtype, p->c.nv,
-                                     (int)varlen * 4 + (int)p->ring * 2 + (int)p->full, p->c.tpb);
+                                     (int)varlen * 8 + p->ring * 2 + (int)p->full, p->c.tpb);
     std::pair<int, int> cached{0, 0};  // (stages, CTAs per SM)
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -123,7 +120,8 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
         auto occupancy = [&](size_t smem, int* bps) {
             return kind == kFwd
                        ? fwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring, p->full, p->c.tpb, smem, bps)
-                       : bwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring, p->full, p->c.tpb, smem, bps);
+                       : bwd_blocks_per_sm((int)dtype, p->c.nv, varlen, p->ring != kRingNone, p->full,
+                                           p->c.tpb, smem, bps);
         };
         int stages = 0, bps = 0;
         if (p->ring) {
@@ -149,11 +147,30 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
     }
     p->stages = cached.first;
     p->smem = p->ring ? kRingHeader + (size_t)p->stages * round : 0;
-    int64_t G = (int64_t)sms * cached.second;
+    int64_t G = (int64_t)p->sms * cached.second;
     if (G > kMaxCtas) G = kMaxCtas;
-    if (G > R) G = R;
-    if (G < 1) G = 1;
     p->G = G;
+    return true;
+}
+
+// Launch plan: staging mode, ring depth, and row tiles = every resident CTA slot of the
+// device (at most one per row).
+bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, Plan* p) {
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    if (sms <= 0) return false;
+    p->sms = sms;
+    p->c = row_cfg(D, dtype, kind == kFwd);
+    p->ring = kRingBudget / ring_round_bytes(kind, p->c, kRingBulk) >= 2 ? kRingBulk : kRingNone;
+    p->full = p->ring && p->c.full;
+    if (!ring_shape(kind, dtype, varlen, dev, p)) return false;
+    if (kind == kFwd && p->ring == kRingBulk && R >= kCopyRingRows * p->G &&
+        kRingBudget / ring_round_bytes(kind, p->c, kRingCopy) >= 2) {
+        p->ring = kRingCopy;
+        if (!ring_shape(kind, dtype, varlen, dev, p)) return false;
+    }
+    if (p->G > R) p->G = R;
+    if (p->G < 1) p->G = 1;
     return true;
 }
 
@@ -269,7 +286,7 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
     a.header = reinterpret_cast<WsHeader*>(base);
     a.stages = p.stages;
     if (stages & kPartials) {
-        if (int rc = launched(launch_bwd(a, (int)dtype, p.c.nv, varlen, p.ring, p.full, G, p.c.tpb,
+        if (int rc = launched(launch_bwd(a, (int)dtype, p.c.nv, varlen, p.ring != kRingNone, p.full, G, p.c.tpb,
                                          p.smem, stream)))
             return rc;
     }

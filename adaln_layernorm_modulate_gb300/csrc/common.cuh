@@ -11,6 +11,7 @@ namespace adaln {
 constexpr int kMaxCtas = 4096;      // upper bound on the row-tile count of one launch
 constexpr int kStage2Threads = 256;
 constexpr int kMaxStages = 8;       // deepest shared-memory ring, in rounds
+enum : int { kRingNone = 0, kRingBulk = 1, kRingCopy = 2 };  // forward staging modes
 
 // A CTA processes its rows in rounds of kRows rows, each thread owning NV 16-byte column
 // vectors of every row. Wider per-thread slices hold fewer rows per round so the values

@@ -7,12 +7,18 @@
 // in registers and the three passes (sum, centred sum of squares, modulated write) run
 // over registers, touching HBM once for x and once for y.
 //
-// Memory-level parallelism: in the ring variant one thread copies whole rows into a
-// shared-memory ring of `stages` rounds with bulk (TMA) copies, one instruction per row,
-// completing on a per-slot mbarrier; it refills a slot as soon as the CTA's first barrier
-// of the round shows every thread has read it. The plain variant, used when a row is too
-// wide for a ring of two rounds, loads straight into registers. FULL: the CTA's threads
-// cover the row exactly (no idle vector slots), so no lane masking is needed.
+// Memory-level parallelism, three staging modes:
+//  - bulk ring: one thread copies whole rows into a shared-memory ring of `stages` rounds
+//    with bulk (TMA) copies, one instruction per row, completing on a per-slot mbarrier; it
+//    refills the previous round's slot at the top of each round, when every thread has
+//    passed that round's barriers. It gets rows flowing fastest after launch: the choice
+//    for short tiles.
+//  - copy ring: every thread copies its own 16-byte vectors (and the row's first word) of
+//    the round `stages` ahead with cp.async and waits only on its own copy groups: no
+//    single producer on the CTA's critical path. It sustains a few percent more bandwidth
+//    on long tiles.
+//  - plain: rows too wide for a ring of two rounds load straight into registers.
+// FULL: the CTA's threads cover the row exactly (no idle vector slots), so no lane masking.
 //
 // Variance: sum and centred sum of squares of d = x - x[row, 0]. Subtracting the row's
 // first element first (shifted data, Chan, Golub & LeVeque 1983) keeps the fp32 sums of
@@ -23,8 +29,9 @@
 
 namespace adaln {
 
-template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
+template <typename T, int NV, bool VARLEN, int RING, bool FULL>
 __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const FwdArgs a) {
+    constexpr bool BULK = RING == kRingBulk, COPY = RING == kRingCopy;
     using IO = Io<T>;
     constexpr int VE = IO::VE;
     constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector
@@ -47,9 +54,10 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
     const float invD = 1.0f / (float)D;
     const int ns = a.stages;
 
-    // Ring layout (32-bit shared addresses): ns mbarriers (first 128 bytes), then [ns][RB]
-    // rows, each row at the offsets it has in global memory (thread t's vector k at
-    // (t + k*TPB)*16), so a bulk copy lands every thread's vectors where it reads them.
+    // Ring layout (32-bit shared addresses): ns mbarriers (first 128 bytes, bulk ring), then
+    // [ns][RB] rows, each row at the offsets it has in global memory (thread t's vector k at
+    // (t + k*TPB)*16), so a bulk copy lands every thread's vectors where it reads them; the
+    // copy ring then keeps [ns][RB][TPB] words, each thread's copy of the row's first word.
     __shared__ int abort_flag;
     const uint32_t vk = (uint32_t)TPB * 16u;           // one vector index k across the CTA
     const uint32_t vrow = (uint32_t)NV * vk;           // one row slot
@@ -57,11 +65,13 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
     const uint32_t bars = smem_addr(ring);
     const uint32_t data = bars + 128u;
     const uint32_t my_vec = data + (uint32_t)tid * 16u;
+    const uint32_t krow = (uint32_t)TPB * 4u, kslot = (uint32_t)RB * krow;
+    const uint32_t my_k = data + (uint32_t)ns * vslot + (uint32_t)tid * 4u;
 
     zero_absent_warps<RB>(red1, nwarps);
     zero_absent_warps<RB>(red2, nwarps);
     uint32_t err = validate_segments<VARLEN>(a.seg, b, G);
-    if constexpr (RING) {
+    if constexpr (BULK) {
         if (tid == 0) {
             for (int q = 0; q < ns; ++q) mbar_init(bars + 8u * q, 1);
             abort_flag = 0;
@@ -81,7 +91,7 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
 
     const int64_t s0 = R > 0 ? seg_find<VARLEN>(a.seg, r0) : 0;
     Walker<VARLEN, RB> cw{r0, s0, -1, false};
-    Walker<VARLEN, RB> pw{r0, s0, -1, false};  // producer's walker (thread 0), ns rounds ahead
+    Walker<VARLEN, RB> pw{r0, s0, -1, false};  // the copies' walker, ns rounds ahead
 
     // Thread 0: copy the producer walker's next round into ring slot `slot`.
     auto issue = [&](int slot) {
@@ -97,9 +107,30 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
                               (uint32_t)row_bytes, bar);
         }
     };
-    if constexpr (RING) {
+    // Copy ring: this thread's vectors of the walker's next round into ring slot `slot`.
+    auto prefetch = [&](int slot) {
+        int64_t rs, sg;
+        int nr;
+        if (pw.next(a.seg, r1, rs, nr, sg)) {
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                if (i >= nr) continue;
+                const char* src = xb + (rs + i) * row_bytes;
+                const uint32_t dst = my_vec + (uint32_t)slot * vslot + (uint32_t)i * vrow;
+                cp_async4_sa(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow, src);
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
+                    if (ok[k]) cp_async16_sa(dst + (uint32_t)k * vk, src + colb[k]);
+            }
+        }
+        cp_async_commit();
+    };
+    if constexpr (BULK) {
         if (tid == 0)
             for (int q = 0; q < ns; ++q) issue(q);
+    }
+    if constexpr (COPY) {
+        for (int q = 0; q < ns; ++q) prefetch(q);
     }
 
     int slot = 0;
@@ -113,7 +144,7 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
     while (cw.next(a.seg, r1, row, nr, s)) {
         uint4 xv[RB][NV];
         float K[RB];
-        if constexpr (RING) {
+        if constexpr (BULK) {
             // The previous round's slot has been read by every thread (they all passed that
             // round's barriers): refill it ns rounds ahead before waiting on this one.
             if (tid == 0 && started) issue(slot == 0 ? ns - 1 : slot - 1);
@@ -126,6 +157,17 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
                 for (int k = 0; k < NV; ++k)
                     xv[i][k] = (i < nr && ok[k]) ? lds128(my_vec + rowsa + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
                 K[i] = (i < nr) ? IO::first_of_word(lds32(data + rowsa)) : 0.0f;
+            }
+        } else if constexpr (COPY) {
+            cp_async_wait(ns - 1);  // this thread's copies of this round have landed
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const uint32_t src = my_vec + (uint32_t)slot * vslot + (uint32_t)i * vrow;
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
+                    xv[i][k] = (i < nr && ok[k]) ? lds128(src + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                K[i] = (i < nr) ? IO::first_of_word(lds32(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow))
+                                : 0.0f;
             }
         } else {
 #pragma unroll
@@ -235,16 +277,21 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
                 }
             }
         }
-        if constexpr (RING) {
+        if constexpr (BULK) {
             if (!cur_ok) __syncthreads();  // a skipped round still fences the slot's readers
             if (++slot == ns) {
                 slot = 0;
                 ++lap;
             }
         }
+        if constexpr (COPY) {
+            prefetch(slot);  // this slot's data is in my registers: refill it ns rounds ahead
+            slot = slot + 1 == ns ? 0 : slot + 1;
+        }
     }
     if (cw.bad) err |= kErrSeqlens;
-    if constexpr (RING) {
+    if constexpr (COPY) cp_async_wait_all();
+    if constexpr (BULK) {
         // After a timed-out wait, copies may still be in flight into this CTA's shared
         // memory: give each slot's outstanding phase one more bounded wait before exiting.
         __syncthreads();
@@ -260,20 +307,23 @@ __global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const Fw
     publish_status(err, a.status, a.header);
 }
 
-template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
+template <typename T, int NV, bool VARLEN, int RING, bool FULL>
 static const void* fwd_fn() {
     return reinterpret_cast<const void*>(&fwd_kernel<T, NV, VARLEN, RING, FULL>);
 }
 
-// Instantiated variants: ring + full row, ring + partial row, plain (partial row).
+// Instantiated variants: each ring with a full or a partial row, plain (partial row).
 template <typename T, int NV, bool VARLEN>
-static const void* pick_variant(bool ring, bool full) {
-    if (ring) return full ? fwd_fn<T, NV, VARLEN, true, true>() : fwd_fn<T, NV, VARLEN, true, false>();
-    return fwd_fn<T, NV, VARLEN, false, false>();
+static const void* pick_variant(int ring, bool full) {
+    if (ring == kRingBulk)
+        return full ? fwd_fn<T, NV, VARLEN, kRingBulk, true>() : fwd_fn<T, NV, VARLEN, kRingBulk, false>();
+    if (ring == kRingCopy)
+        return full ? fwd_fn<T, NV, VARLEN, kRingCopy, true>() : fwd_fn<T, NV, VARLEN, kRingCopy, false>();
+    return fwd_fn<T, NV, VARLEN, kRingNone, false>();
 }
 
 template <typename T, bool VARLEN>
-static const void* pick_nv(int nv, bool ring, bool full) {
+static const void* pick_nv(int nv, int ring, bool full) {
     switch (nv) {
         case 1: return pick_variant<T, 1, VARLEN>(ring, full);
         case 2: return pick_variant<T, 2, VARLEN>(ring, full);
@@ -285,7 +335,7 @@ static const void* pick_nv(int nv, bool ring, bool full) {
     }
 }
 
-static const void* pick_fwd(int dtype, int nv, bool varlen, bool ring, bool full) {
+static const void* pick_fwd(int dtype, int nv, bool varlen, int ring, bool full) {
     if (dtype == 0) return varlen ? pick_nv<float, true>(nv, ring, full) : pick_nv<float, false>(nv, ring, full);
     if (dtype == 1)
         return varlen ? pick_nv<__nv_bfloat16, true>(nv, ring, full)
@@ -293,7 +343,7 @@ static const void* pick_fwd(int dtype, int nv, bool varlen, bool ring, bool full
     return nullptr;
 }
 
-cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
+cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, int ring, bool full, int tpb,
                               size_t smem, int* out) {
     const void* fn = pick_fwd(dtype, nv, varlen, ring, full);
     if (!fn) return cudaErrorInvalidValue;
@@ -302,7 +352,7 @@ cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool fu
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, fn, tpb, smem);
 }
 
-cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
+cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, int ring, bool full,
                        int64_t G, int tpb, size_t smem, cudaStream_t stream) {
     const void* fn = pick_fwd(dtype, nv, varlen, ring, full);
     if (!fn) return cudaErrorInvalidValue;

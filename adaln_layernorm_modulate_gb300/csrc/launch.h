@@ -7,11 +7,12 @@
 
 namespace adaln {
 
-// `ring`: the cp.async shared-memory ring variant; `full`: the CTA covers the row exactly
-// (ring variant only); `smem`: the ring's dynamic shared memory bytes.
-cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
+// Forward `ring`: kRingNone, kRingBulk or kRingCopy; backward `ring`: the bulk ring or
+// none. `full`: the CTA covers the row exactly (ring variants only); `smem`: the ring's
+// dynamic shared memory bytes.
+cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, int ring, bool full, int tpb,
                               size_t smem, int* out);
-cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
+cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, int ring, bool full,
                        int64_t G, int tpb, size_t smem, cudaStream_t stream);
 
 cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
