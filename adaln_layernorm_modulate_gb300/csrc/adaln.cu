@@ -77,9 +77,10 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
 
 enum Kind { kFwd = 0, kBwd = 1 };
 
-// Most shared memory a CTA gives its ring (two such CTAs fit on one SM); less when
-// registers let more CTAs share the SM.
-constexpr size_t kRingBudget = 100 * 1024;
+// Most shared memory a CTA gives its ring; less when registers let more CTAs share the
+// SM. A CTA alone on its SM (wide rows in the backward) stops at 150 KB: deeper rings
+// measured slower, the rest of the SM's shared memory serving as L1.
+constexpr size_t kRingBudget = 150 * 1024;
 // Forward tiles at least this many rows long stage rows with the per-thread copy ring,
 // shorter ones with the bulk ring (which starts faster, see fwd.cu).
 constexpr int64_t kCopyRingRows = 256;
@@ -174,10 +175,10 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
     return true;
 }
 
-// float4 columns per stage-2 CTA: aim for ~4 CTAs per SM over all modulation rows.
+// float4 columns per stage-2 CTA: aim for ~2 CTAs per SM over all modulation rows.
 int stage2_cw(int64_t D, int64_t nmod, int sms) {
     const int64_t D4 = D / 4;
-    const int64_t target = 4 * (int64_t)sms;
+    const int64_t target = 2 * (int64_t)sms;
     const int64_t ranges = (target + nmod - 1) / (nmod > 0 ? nmod : 1);
     const int64_t per = (D4 + ranges - 1) / ranges;
     int cw = 1;
