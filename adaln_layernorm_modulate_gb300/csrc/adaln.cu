@@ -57,7 +57,11 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
     int64_t target = (forward ? 32 : 16) / VE;
     if ((V + 31) / 32 < target) target = (V + 31) / 32;
     if (target < 1) target = 1;
-    // First choice: a mapping that covers the row exactly (whole warps, no idle lanes),
+    // Forward rows of at most 6 vectors per lane: one warp per row. The CTA's reductions are
+    // then warp shuffles and its barriers cover one warp, so the rows of different warps
+    // never wait for each other (bf16 D=1536: 33 us against 36 us for 3 x 64 threads).
+    if (forward && V % 32 == 0 && V / 32 <= 6 && V / 32 != 5) return RowCfg{(int)(V / 32), 32, true};
+    // Otherwise a mapping that covers the row exactly (whole warps, no idle lanes),
     // with nv as close to the target as possible (ties go to the smaller nv).
     int best = 0;
     for (int nv : kNv) {
