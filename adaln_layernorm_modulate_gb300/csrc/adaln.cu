@@ -50,19 +50,32 @@ struct RowCfg {
 
 int max_threads_for(int nv) { return nv == 1 || nv >= 8 ? 512 : 384; }
 
-RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
+// Row mapping of a launch. `copy_ring`: the forward will stage rows with the per-thread
+// copy ring (long tiles), otherwise with the bulk ring or plain loads. The preferences were
+// measured on GB300 (bf16 D=3072 forward: 3 x 128 threads with the copy ring, 992 us on the
+// packed workload against 1035 us for 4 x 96; 6 x 64 threads with the bulk ring, 67.9 us on
+// a 32,760-token segment against 70.6 us).
+RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward, bool copy_ring) {
     static const int kNv[] = {1, 2, 3, 4, 6, 8};
-    const int64_t VE = dtype == ADALN_BF16 ? 8 : 4;
+    const bool bf16 = dtype == ADALN_BF16;
+    const int64_t VE = bf16 ? 8 : 4;
     const int64_t V = D / VE;
-    int64_t target = (forward ? 32 : 16) / VE;
-    if ((V + 31) / 32 < target) target = (V + 31) / 32;
-    if (target < 1) target = 1;
+    // Copy ring: three vectors a thread (two rows a round) when that covers the row with at
+    // least four warps.
+    if (forward && copy_ring && V % 3 == 0 && (V / 3) % 32 == 0 && V / 3 >= 128 &&
+        V / 3 <= max_threads_for(3))
+        return RowCfg{3, (int)(V / 3), true};
     // Forward rows of at most 6 vectors per lane: one warp per row. The CTA's reductions are
     // then warp shuffles and its barriers cover one warp, so the rows of different warps
     // never wait for each other (bf16 D=1536: 33 us against 36 us for 3 x 64 threads).
     if (forward && V % 32 == 0 && V / 32 <= 6 && V / 32 != 5) return RowCfg{(int)(V / 32), 32, true};
-    // Otherwise a mapping that covers the row exactly (whole warps, no idle lanes),
-    // with nv as close to the target as possible (ties go to the smaller nv).
+    // Elements a thread: the backward keeps x, dy and two column accumulators per element,
+    // the forward one value (bf16 forwards take 48, the others 32).
+    int64_t target = (forward ? (bf16 ? 48 : 32) : 16) / VE;
+    if ((V + 31) / 32 < target) target = (V + 31) / 32;
+    if (target < 1) target = 1;
+    // Otherwise a mapping that covers the row exactly (whole warps, no idle lanes), with nv
+    // as close to the target as possible (ties go to the smaller nv).
     int best = 0;
     for (int nv : kNv) {
         if (V % nv != 0 || (V / nv) % 32 != 0 || V / nv > max_threads_for(nv)) continue;
@@ -165,14 +178,18 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
     const int sms = current_sms(&dev);
     if (sms <= 0) return false;
     p->sms = sms;
-    p->c = row_cfg(D, dtype, kind == kFwd);
+    p->c = row_cfg(D, dtype, kind == kFwd, false);
     p->ring = kRingBudget / ring_round_bytes(kind, p->c, kRingBulk) >= 2 ? kRingBulk : kRingNone;
     p->full = p->ring && p->c.full;
     if (!ring_shape(kind, dtype, varlen, dev, p)) return false;
-    if (kind == kFwd && p->ring == kRingBulk && R >= kCopyRingRows * p->G &&
-        kRingBudget / ring_round_bytes(kind, p->c, kRingCopy) >= 2) {
-        p->ring = kRingCopy;
-        if (!ring_shape(kind, dtype, varlen, dev, p)) return false;
+    if (kind == kFwd && p->ring == kRingBulk && R >= kCopyRingRows * p->G) {
+        const RowCfg copy = row_cfg(D, dtype, true, true);
+        if (kRingBudget / ring_round_bytes(kind, copy, kRingCopy) >= 2) {
+            p->c = copy;
+            p->ring = kRingCopy;
+            p->full = copy.full;
+            if (!ring_shape(kind, dtype, varlen, dev, p)) return false;
+        }
     }
     if (p->G > R) p->G = R;
     if (p->G < 1) p->G = 1;
