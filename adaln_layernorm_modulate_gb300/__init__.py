@@ -30,7 +30,8 @@ EXPORTS = (
     "adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd", "adaln_bwd_partials", "adaln_bwd_reduce",
     "adaln_fwd_varlen_workspace_size", "adaln_fwd_varlen", "adaln_bwd_varlen_workspace_size",
     "adaln_bwd_varlen", "adaln_bwd_varlen_partials", "adaln_bwd_varlen_reduce",
-    "adaln_read_status", "adaln_bwd_noalloc", "adaln_bucket_batch", "adaln_status_string",
+    "adaln_read_status", "adaln_bwd_noalloc", "adaln_bucket_batch", "adaln_bucket_batch_real",
+    "adaln_fit_step_cost", "adaln_bucket_load_cv", "adaln_status_string",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ADALN_NOALLOC_SCRATCH_BYTES
 
@@ -68,6 +69,10 @@ def _load() -> ctypes.CDLL:
         "adaln_read_status": ([vp, vp], ci),
         "adaln_bwd_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp], ci),
         "adaln_bucket_batch": ([i64, i64, i64, i32], i64),
+        "adaln_bucket_batch_real": ([i64, i64, i64, ctypes.c_double], i64),
+        "adaln_fit_step_cost": ([vp, vp, vp, i64, ctypes.c_double, ctypes.c_double,
+                                 ctypes.c_double, vp], ci),
+        "adaln_bucket_load_cv": ([vp, i64, vp, i32, i64, i64, ctypes.c_double, i32, vp], ci),
         "adaln_status_string": ([ci], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
@@ -216,6 +221,40 @@ def adaln_bwd_noalloc(dy, x, mean, rstd, scale, dx, dshift, dscale, Bt, N, D, dt
 
 def adaln_bucket_batch(S, M_mem, M_comp, p) -> int:
     return int(lib().adaln_bucket_batch(S, M_mem, M_comp, p))
+
+
+def _host_array(values, ctype):
+    arr = (ctype * len(values))(*values)
+    return arr, ctypes.cast(arr, ctypes.c_void_p).value
+
+
+def adaln_bucket_batch_real(S, M_mem, M_comp, p) -> int:
+    return int(lib().adaln_bucket_batch_real(S, M_mem, M_comp, float(p)))
+
+
+def adaln_fit_step_cost(B, S, t, p_lo=1.0, p_hi=3.0, t_budget=0.0) -> dict:
+    """Host arrays (sequences) of equal length n; returns a, b, p, rms, M_comp."""
+    n = len(t)
+    if len(B) != n or len(S) != n:
+        raise ValueError("B, S and t must have one length")
+    b_arr, b_p = _host_array([int(v) for v in B], ctypes.c_int64)
+    s_arr, s_p = _host_array([int(v) for v in S], ctypes.c_int64)
+    t_arr, t_p = _host_array([float(v) for v in t], ctypes.c_double)
+    out = (ctypes.c_double * 5)()
+    _check("adaln_fit_step_cost", lib().adaln_fit_step_cost(
+        b_p, s_p, t_p, n, float(p_lo), float(p_hi), float(t_budget), ctypes.cast(out, ctypes.c_void_p)))
+    return {"a": out[0], "b": out[1], "p": out[2], "rms": out[3], "M_comp": out[4]}
+
+
+def adaln_bucket_load_cv(lengths, buckets, M_mem, M_comp, p, rule) -> dict:
+    """rule 0: equal-token batches; rule 1: dual constraint. Returns cv, batches, mean."""
+    l_arr, l_p = _host_array([int(v) for v in lengths], ctypes.c_int64)
+    k_arr, k_p = _host_array([int(v) for v in buckets], ctypes.c_int64)
+    out = (ctypes.c_double * 3)()
+    _check("adaln_bucket_load_cv", lib().adaln_bucket_load_cv(
+        l_p, len(lengths), k_p, len(buckets), M_mem, M_comp, float(p), int(rule),
+        ctypes.cast(out, ctypes.c_void_p)))
+    return {"cv": out[0], "batches": int(out[1]), "mean": out[2]}
 
 
 def adaln_status_string(status) -> str:

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "adaln")
 LIB = os.path.join(PKG, "libadaln.so")
-SOURCES = ["adaln.cu", "fwd.cu", "bwd.cu"]
+SOURCES = ["adaln.cu", "fwd.cu", "bwd.cu", "schedule.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -190,6 +190,41 @@ int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean, const fl
  * Returns B >= 1, or -ADALN_ERR_INVALID_ARG when S, M_mem or M_comp <= 0 or p < 1. */
 int64_t adaln_bucket_batch(int64_t S, int64_t M_mem, int64_t M_comp, int32_t p);
 
+/* ---- Host-side scheduling half of section 2.A (host only, no device work) ------------- */
+
+/* adaln_bucket_batch with a real exponent p > 0, as a fitted exponent is. An integral p in
+ * [1, 64] takes the exact integer path; otherwise S^p is evaluated in double precision and
+ * floor(M_comp / S^p) can differ by one from the exact value when M_comp / S^p lies within
+ * about 1e-13 (relative) of an integer. Returns B >= 1, or -ADALN_ERR_INVALID_ARG when S,
+ * M_mem or M_comp <= 0 or p is not positive and finite. */
+int64_t adaln_bucket_batch_real(int64_t S, int64_t M_mem, int64_t M_comp, double p);
+
+/* Shape-Benchmarking cost fit, section 2.A: the least-squares fit of the step-time model
+ *     t = a + b * B * S^p
+ * to n measured (B[i], S[i], t[i]) samples, p searched in [p_lo, p_hi] (for each p the
+ * model is linear in a and b, solved exactly; the residual is then minimised over p by a
+ * grid bracket and golden-section refinement to 1e-12 in p). With a step-time budget
+ * t_budget > a, the compute bound follows as M_comp = floor((t_budget - a) / b).
+ * Writes out[0..4] = a, b, p, root-mean-square residual, M_comp (M_comp = 0 when
+ * t_budget <= a or b <= 0). Returns ADALN_OK, or ADALN_ERR_INVALID_ARG for n < 3, a null
+ * pointer, B or S <= 0, a non-finite t, or not 0 < p_lo < p_hi. */
+int adaln_fit_step_cost(const int64_t* B, const int64_t* S, const double* t, int64_t n,
+                        double p_lo, double p_hi, double t_budget, double* out);
+
+/* Compute-load imbalance of a bucketing rule, the quantity section 2.A's scheduler lowers
+ * (the results report its coefficient of variation across batches). Each of the n sample
+ * lengths goes to the smallest of the nbuckets increasing bucket lengths that holds it; a
+ * bucket's samples, in input order, fill batches of its batch size, the last one possibly
+ * partial. Batch size: rule 0 = the equal-token rule max(1, floor(M_mem / S)); rule 1 =
+ * the dual constraint adaln_bucket_batch_real(S, M_mem, M_comp, p). A batch of k samples of
+ * bucket S costs k * S^p. Writes out[0..2] = coefficient of variation (population standard
+ * deviation / mean) of the batch costs, number of batches, mean cost. Returns ADALN_OK, or
+ * ADALN_ERR_INVALID_ARG for a null pointer, n < 1, nbuckets < 1, buckets not increasing and
+ * positive, a length <= 0 or above the largest bucket, M_mem or M_comp <= 0, a bad p or rule. */
+int adaln_bucket_load_cv(const int64_t* lengths, int64_t n, const int64_t* buckets,
+                         int32_t nbuckets, int64_t M_mem, int64_t M_comp, double p, int32_t rule,
+                         double* out);
+
 /* Static, human-readable name of a status code. */
 const char* adaln_status_string(int status);
 
