@@ -56,6 +56,8 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="packed")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-chunks", type=int, default=8,
+                   help="segment chunks of the pipelined end-to-end step (1: serial)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -309,6 +311,96 @@ def run_reference(args):
 # ------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------
+def e2e_chunks(w: synth.Workload, n: int):
+    """Split a packed batch into about n chunks of consecutive segments for the end-to-end
+    pipeline, or None if the chunks' modulation rows would not be contiguous, disjoint and
+    covering (every table row must be written by exactly one chunk's backward)."""
+    if w.dense is not None or w.nseg < 2:
+        return None
+    mod = np.asarray(w.mod_idx)
+    if w.nmod != w.nseg or not np.array_equal(mod, np.arange(w.nseg)):
+        return None
+    cu = np.asarray(w.cu_seqlens)
+    cuts = sorted(set(int(np.searchsorted(cu, w.R * i / n)) for i in range(1, n)) - {0, w.nseg})
+    bounds = [0] + cuts + [w.nseg]
+    return [(s0, s1) for s0, s1 in zip(bounds[:-1], bounds[1:]) if s1 > s0]
+
+
+def chunked_e2e_step(A, w, chunks, pin, out_h, d, outs, sptr, shape_batch, dev):
+    """One end-to-end step over segment chunks: chunk c's inputs go up on a copy stream, its
+    forward and backward run on the compute stream once they have landed, and its outputs
+    come down on a third stream, so copies in both directions overlap the kernels and each
+    other. Each chunk is a packed call on its own segments and table rows."""
+    import torch
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    cu = np.asarray(w.cu_seqlens)
+    plan = []
+    ws_f = ws_b = 0
+    for s0, s1 in chunks:
+        t0, t1 = int(cu[s0]), int(cu[s1])
+        local_cu = torch.from_numpy((cu[s0:s1 + 1] - t0).astype(np.int32)).pin_memory()
+        local_mod = torch.from_numpy(np.arange(s1 - s0, dtype=np.int32)).pin_memory()
+        R, nseg = t1 - t0, s1 - s0
+        ws_f = max(ws_f, A.adaln_fwd_varlen_workspace_size(R, nseg, w.D, w.dtype))
+        ws_b = max(ws_b, A.adaln_bwd_varlen_workspace_size(R, nseg, nseg, w.D, w.dtype))
+        plan.append((s0, s1, t0, t1, local_cu, local_mod,
+                     torch.empty(s1 - s0 + 1, dtype=torch.int32, device=dev),
+                     torch.empty(s1 - s0, dtype=torch.int32, device=dev)))
+    wsf = torch.empty(ws_f, dtype=torch.uint8, device=dev)
+    wsb = torch.empty(ws_b, dtype=torch.uint8, device=dev)
+    rows = ("x", "dy")
+    tables = ("shift", "scale")
+    out_rows = ("y", "dx", "mean", "rstd")
+    out_tables = ("dshift", "dscale")
+    state = {"last_compute": None, "last_out": None}
+
+    def step():
+        shape_batch()
+        begin = torch.cuda.Event()
+        begin.record(comp)
+        s_in.wait_event(begin)  # nothing of this step starts before what precedes it on comp
+        if state["last_compute"] is not None:
+            s_in.wait_event(state["last_compute"])  # inputs are overwritten only once read
+            comp.wait_event(state["last_out"])      # outputs only once copied down
+        for s0, s1, t0, t1, hcu, hmod, dcu, dmod in plan:
+            with torch.cuda.stream(s_in):
+                for k in rows:
+                    d[k][t0:t1].copy_(pin[k][t0:t1], non_blocking=True)
+                for k in tables:
+                    d[k][s0:s1].copy_(pin[k][s0:s1], non_blocking=True)
+                dcu.copy_(hcu, non_blocking=True)
+                dmod.copy_(hmod, non_blocking=True)
+                landed = torch.cuda.Event()
+                landed.record(s_in)
+            comp.wait_event(landed)
+            R, nseg = t1 - t0, s1 - s0
+            A.adaln_fwd_varlen(d["x"][t0:t1], d["shift"][s0:s1], d["scale"][s0:s1], outs["y"][t0:t1],
+                               outs["mean"][t0:t1], outs["rstd"][t0:t1], dcu, dmod, nseg, R, nseg, w.D,
+                               EPS, wsf, ws_f, w.dtype, sptr)
+            A.adaln_bwd_varlen(d["dy"][t0:t1], d["x"][t0:t1], outs["mean"][t0:t1], outs["rstd"][t0:t1],
+                               d["scale"][s0:s1], outs["dx"][t0:t1], outs["dshift"][s0:s1],
+                               outs["dscale"][s0:s1], dcu, dmod, nseg, R, nseg, w.D, wsb, ws_b,
+                               w.dtype, sptr)
+            done = torch.cuda.Event()
+            done.record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                for k in out_rows:
+                    out_h[k][t0:t1].copy_(outs[k][t0:t1], non_blocking=True)
+                for k in out_tables:
+                    out_h[k][s0:s1].copy_(outs[k][s0:s1], non_blocking=True)
+        state["last_compute"] = torch.cuda.Event()
+        state["last_compute"].record(comp)
+        state["last_out"] = torch.cuda.Event()
+        state["last_out"].record(s_out)
+        comp.wait_event(state["last_out"])  # the step ends when its last copy has landed
+
+    step.h2d_bytes = sum(pin[k].element_size() * pin[k].numel() for k in rows + tables) + sum(
+        (c[4].numel() + c[5].numel()) * 4 for c in plan)
+    return step
+
+
 def run_ours(args):
     import torch
 
@@ -468,6 +560,10 @@ def run_ours(args):
             for k, v in out_h.items():
                 v.copy_(outs[k], non_blocking=True)
 
+        chunks = e2e_chunks(w, args.e2e_chunks) if args.e2e_chunks > 1 else None
+        if chunks is not None:
+            e2e_step = chunked_e2e_step(A, w, chunks, pin, out_h, d, outs, sptr, shape_batch, dev)
+            h2d = e2e_step.h2d_bytes
         e2e_step()
         torch.cuda.synchronize()
         a, b = events(2)
@@ -480,7 +576,9 @@ def run_ours(args):
         barrier(dist)
         e2e_ms = max_over_ranks(dist, a.elapsed_time(b) / args.e2e_steps)
         e2e = {"value": world * nb["step"] / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "pipeline": ("%d segment chunks; host-to-device copies, kernels and device-to-host "
+                            "copies on three streams" % len(chunks)) if chunks else "serial"}
 
     if rank != 0:
         return 0
