@@ -200,16 +200,7 @@ struct Walker {
 // Asynchronous global -> shared copies issued per thread. Completion is tracked per thread
 // with commit/wait groups and each thread reads back only what it copied itself, so no
 // cross-thread synchronisation (and no waiting on anyone else) is involved.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-// 4-byte copy through L1 (the threads of a CTA fetch the same word: one L1 line).
-__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
-}
-// The same copies addressed by 32-bit shared-window addresses (cheaper index math).
+// Copies are addressed by 32-bit shared-window addresses (cheaper index math).
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -325,46 +316,7 @@ inline cudaError_t allow_dynamic_smem(const void* fn) {
 // Packed fp32 pairs: Blackwell's f32x2 ALU instructions. Each lane of a pair is rounded
 // exactly as the scalar instruction would round it.
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
-
-// The same pair operations on a pair held in one 64-bit register (low half = element 2p,
-// high half = element 2p+1). Keeping pairs in this form end to end lets the compiler feed
+// A pair is held in one 64-bit register (low half = element 2p, high half = element 2p+1). Keeping pairs in this form end to end lets the compiler feed
 // the f32x2 instructions without repacking 32-bit halves around every operation.
 using f2r = unsigned long long;
 __device__ __forceinline__ f2r p_add(f2r a, f2r b) {
@@ -390,11 +342,6 @@ __device__ __forceinline__ f2r p_fma(f2r a, f2r b, f2r c) {
 __device__ __forceinline__ f2r p_splat(float v) {
     f2r d;
     asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(v));
-    return d;
-}
-__device__ __forceinline__ f2r p_make(float lo, float hi) {
-    f2r d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
     return d;
 }
 __device__ __forceinline__ float2 p_get(f2r a) {
@@ -452,15 +399,6 @@ struct Io;
 template <>
 struct Io<float> {
     static constexpr int VE = 4;  // elements per 16-byte vector
-    // As VE/2 fp32 pairs (element 2p in .x, 2p+1 in .y).
-    __device__ static __forceinline__ void unpack2(const uint4& v, float2* f) {
-        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
-        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
-    }
-    __device__ static __forceinline__ uint4 pack2v(const float2* f) {
-        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
-                          __float_as_uint(f[1].y));
-    }
     __device__ static __forceinline__ float first(const void* p) {
         return __ldg(reinterpret_cast<const float*>(p));
     }
@@ -483,20 +421,6 @@ template <>
 struct Io<__nv_bfloat16> {
     static constexpr int VE = 8;
     // bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 pattern.
-    __device__ static __forceinline__ void unpack2(const uint4& v, float2* f) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            f[j] = make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
-    }
-    __device__ static __forceinline__ uint32_t pack_pair(float lo, float hi) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-    __device__ static __forceinline__ uint4 pack2v(const float2* f) {
-        return make_uint4(pack_pair(f[0].x, f[0].y), pack_pair(f[1].x, f[1].y),
-                          pack_pair(f[2].x, f[2].y), pack_pair(f[3].x, f[3].y));
-    }
     __device__ static __forceinline__ float first(const void* p) {
         const uint32_t h = __ldg(reinterpret_cast<const unsigned short*>(p));
         return __uint_as_float(h << 16);
