@@ -108,6 +108,11 @@ SMALL = {
         "c", 115, synth.BF16, 8, [400000, 3, 700000], [1, 0, 1], 2,
         x_mode=synth.ROWS_SCALED, dy_std=0.02),
     "dense-f32-d16-long-tiles": lambda: synth.dense("c", 116, synth.F32, 2, 600000, 16),
+    # Many modulation rows over a 700-segment table: rows shared by several segments, rows
+    # no segment uses (zero gradients), stage 2 over 2 column blocks x 601 rows.
+    "packed-f32-d2048-601rows": lambda: synth.make(
+        "c", 117, synth.F32, 2048, list(np.random.default_rng(12).integers(0, 30, 700)),
+        list(np.random.default_rng(13).integers(0, 601, 700)), 601, dy_std=0.5),
     # One long segment spread over many row tiles, sharing its modulation row with
     # thousands of short ones.
     "packed-bf16-d256-long-and-many": lambda: synth.make(
