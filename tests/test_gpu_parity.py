@@ -196,6 +196,14 @@ def test_full_packed_buckets(orc):
     _full_size(orc, w, [0, 511, 512, 639, 640, 671, 673, 674, 675])
 
 
+def test_full_bucket_s32760(orc):
+    # The packed workload's S=32760 bucket as its own call (one segment spanning every tile).
+    import adaln_layernorm_modulate_gb300 as A
+    w = synth.bucket(32760, A.adaln_bucket_batch)
+    assert w.nseg == 1 and w.R == 32760
+    _full_size(orc, w, [0])
+
+
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16], ids=["f32", "bf16"])
 def test_full_mmdit(orc, dtype):
     _full_size(orc, synth.config(4, dtype=dtype), [0, 1, 2, 3])
