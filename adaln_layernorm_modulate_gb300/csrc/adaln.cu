@@ -42,14 +42,13 @@ int current_sms(int* dev_out) {
 // registers run out: the forward holds about 32 elements a thread, the backward (which
 // keeps twice as many values per element) about 16. Narrow rows shrink nv so a warp is not
 // left idle; wide rows grow it so a row fits the CTA size the kernel is compiled for
-// (RowShape<nv>::kMaxThreads).
+// (max_threads(nv, elements per vector)).
 struct RowCfg {
     int nv;
     int tpb;
     bool full;  // nv * tpb vectors == the row: no idle lanes
 };
 
-int max_threads_for(int nv) { return nv == 1 || nv >= 8 ? 512 : 384; }
 
 // Row mapping of a launch. `copy_ring`: the forward will stage rows with the per-thread
 // copy ring (long tiles), otherwise with the bulk ring or plain loads. The preferences were
@@ -64,7 +63,7 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward, bool copy_ring) {
     // Copy ring: three vectors a thread (two rows a round) when that covers the row with at
     // least four warps.
     if (forward && copy_ring && V % 3 == 0 && (V / 3) % 32 == 0 && V / 3 >= 128 &&
-        V / 3 <= max_threads_for(3))
+        V / 3 <= max_threads(3, (int)VE))
         return RowCfg{3, (int)(V / 3), true};
     // Forward rows of at most 6 vectors per lane: one warp per row. The CTA's reductions are
     // then warp shuffles and its barriers cover one warp, so the rows of different warps
@@ -79,7 +78,7 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward, bool copy_ring) {
     // as close to the target as possible (ties go to the smaller nv).
     int best = 0;
     for (int nv : kNv) {
-        if (V % nv != 0 || (V / nv) % 32 != 0 || V / nv > max_threads_for(nv)) continue;
+        if (V % nv != 0 || (V / nv) % 32 != 0 || V / nv > max_threads(nv, (int)VE)) continue;
         if (nv > 2 * target) continue;
         if (best == 0 || std::llabs(nv - target) < std::llabs(best - target)) best = nv;
     }
@@ -87,7 +86,7 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward, bool copy_ring) {
     for (int nv : kNv) {
         if (nv < target) continue;
         const int64_t tpb = ((V + nv - 1) / nv + 31) / 32 * 32;
-        if (tpb <= max_threads_for(nv)) return RowCfg{nv, (int)tpb, V == nv * tpb};
+        if (tpb <= max_threads(nv, (int)VE)) return RowCfg{nv, (int)tpb, V == nv * tpb};
     }
     const int64_t tpb = ((V + 7) / 8 + 31) / 32 * 32;
     return RowCfg{8, (int)tpb, V == 8 * tpb};

@@ -21,7 +21,7 @@
 namespace adaln {
 
 template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
-__global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) bwd_kernel(const BwdArgs a) {
     using IO = Io<T>;
     constexpr int VE = IO::VE;
     constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector

@@ -13,16 +13,24 @@ constexpr int kStage2Threads = 256;
 constexpr int kMaxStages = 8;       // deepest shared-memory ring, in rounds
 enum : int { kRingNone = 0, kRingBulk = 1, kRingCopy = 2 };  // forward staging modes
 
+// Largest CTA the host may pick for NV vectors a thread of VE-element vectors. It is the
+// kernels' launch bound, which sets their register budget (65536 / bound a thread): bf16
+// rows of 8 vectors a thread (64 elements; bf16 D <= 16384 needs at most 256 threads) get
+// 255 registers, fp32 ones keep 512 threads for D = 16384.
+__host__ __device__ constexpr int max_threads(int nv, int ve) {
+    return nv == 1 ? 512 : nv >= 8 ? (ve == 8 ? 256 : 512) : 384;
+}
+
 // A CTA processes its rows in rounds of kRows rows, each thread owning NV 16-byte column
 // vectors of every row. Wider per-thread slices hold fewer rows per round so the values
-// stay in registers; kMaxThreads bounds the CTA size the host may pick for that NV.
+// stay in registers.
 template <int NV>
 struct RowShape {
     static constexpr int kRows = NV <= 2 ? 2 : 1;
     // The forward holds one row's values where the backward holds two (x and dy), so it
     // can take two rows a round up to NV = 3.
     static constexpr int kFwdRows = NV <= 3 ? 2 : 1;
-    static constexpr int kMaxThreads = NV == 1 || NV >= 8 ? 512 : 384;
+
 };
 
 // Workspace layout: [header | one status word per CTA | backward partials].

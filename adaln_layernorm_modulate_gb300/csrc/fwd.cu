@@ -30,7 +30,7 @@
 namespace adaln {
 
 template <typename T, int NV, bool VARLEN, int RING, bool FULL>
-__global__ void __launch_bounds__(RowShape<NV>::kMaxThreads) fwd_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const FwdArgs a) {
     constexpr bool BULK = RING == kRingBulk, COPY = RING == kRingCopy;
     using IO = Io<T>;
     constexpr int VE = IO::VE;
