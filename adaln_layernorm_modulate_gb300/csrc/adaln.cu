@@ -98,6 +98,9 @@ enum Kind { kFwd = 0, kBwd = 1 };
 // SM. A CTA alone on its SM (wide rows in the backward) stops at 150 KB: deeper rings
 // measured slower, the rest of the SM's shared memory serving as L1.
 constexpr size_t kRingBudget = 150 * 1024;
+// Rows whose two-round ring exceeds the budget still get one, up to this size (fp32
+// D=12288 backward: two rounds of 96 KB), rather than plain loads into registers.
+constexpr size_t kRingLimit = 200 * 1024;
 // Forward tiles at least this many rows long stage rows with the per-thread copy ring,
 // shorter ones with the bulk ring (which starts faster, see fwd.cu).
 constexpr int64_t kCopyRingRows = 256;
@@ -179,12 +182,13 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
     if (sms <= 0) return false;
     p->sms = sms;
     p->c = row_cfg(D, dtype, kind == kFwd, false);
-    p->ring = kRingBudget / ring_round_bytes(kind, p->c, kRingBulk) >= 2 ? kRingBulk : kRingNone;
+    // A ring needs two rounds; rows too wide for two rounds in kRingLimit load into registers.
+    p->ring = 2 * ring_round_bytes(kind, p->c, kRingBulk) + kRingHeader <= kRingLimit ? kRingBulk : kRingNone;
     p->full = p->ring && p->c.full;
     if (!ring_shape(kind, dtype, varlen, dev, p)) return false;
     if (kind == kFwd && p->ring == kRingBulk && R >= kCopyRingRows * p->G) {
         const RowCfg copy = row_cfg(D, dtype, true, true);
-        if (kRingBudget / ring_round_bytes(kind, copy, kRingCopy) >= 2) {
+        if (2 * ring_round_bytes(kind, copy, kRingCopy) + kRingHeader <= kRingLimit) {
             p->c = copy;
             p->ring = kRingCopy;
             p->full = copy.full;

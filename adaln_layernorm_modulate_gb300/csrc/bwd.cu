@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) bwd_kernel(const B
     constexpr int VE = IO::VE;
     constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector
     constexpr int RB = RowShape<NV>::kRows;
+    // Wide rows read x and dy from the ring twice instead of holding them in registers.
+    constexpr bool REREAD = RING && NV >= 6;
+    static_assert(!REREAD || RB == 1, "wide rows are staged one a round");
     extern __shared__ uint4 ring[];
     __shared__ __align__(16) float red[2][2 * RB][32];  // double-buffered per-warp sums of g, g*xhat
 
@@ -162,14 +165,16 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) bwd_kernel(const B
             if (tid == 0 && started) issue(slot == 0 ? ns - 1 : slot - 1);
             started = true;
             if (!mbar_wait_bounded(bars + 8u * (uint32_t)slot, lap & 1u, &abort_flag)) err |= kErrTimeout;
+            if constexpr (!REREAD) {
 #pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                const uint32_t xs = my_vec + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
+                for (int i = 0; i < RB; ++i) {
+                    const uint32_t xs = my_vec + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
 #pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const bool on = i < nr && ok[k];
-                    xv[i][k] = on ? lds128(xs + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
-                    gv[i][k] = on ? lds128(xs + vrow + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                    for (int k = 0; k < NV; ++k) {
+                        const bool on = i < nr && ok[k];
+                        xv[i][k] = on ? lds128(xs + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                        gv[i][k] = on ? lds128(xs + vrow + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                    }
                 }
             }
         } else {
@@ -204,7 +209,56 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) bwd_kernel(const B
             }
         }
 
-        if (cur_ok) {  // uniform across the CTA
+        if (REREAD && cur_ok) {
+            // Wide rows (RB = 1): x and dy stay in the ring slot. Pass 1 reads them for the row
+            // sums and the column accumulators, pass 2 reads them again for dx, so only the
+            // accumulators and (1 + scale) stay in registers across the row.
+            const uint32_t xs = my_vec + (uint32_t)slot * vslot;
+            const f2r rs2 = p_splat(rs[0]), mu2 = p_splat(mu[0]);
+            f2r sg[2] = {kPairZero, kPairZero}, sgx[2] = {kPairZero, kPairZero};
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const uint4 xq = ok[k] ? lds128(xs + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                const uint4 gq = ok[k] ? lds128(xs + vrow + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                f2r xh[PV], fd[PV];
+                IO::unpackp(xq, xh);
+                IO::unpackp(gq, fd);
+#pragma unroll
+                for (int p = 0; p < PV; ++p) {
+                    xh[p] = p_mul(p_sub(xh[p], mu2), rs2);
+                    const f2r g = p_mul(fd[p], sc1[k][p]);
+                    sg[p & 1] = p_add(sg[p & 1], g);
+                    sgx[p & 1] = p_fma(g, xh[p], sgx[p & 1]);
+                    acc_dy[k][p] = p_add(acc_dy[k][p], fd[p]);
+                    acc_dyx[k][p] = p_fma(fd[p], xh[p], acc_dyx[k][p]);
+                }
+            }
+            float sums[2] = {p_hsum(p_add(sg[0], sg[1])), p_hsum(p_add(sgx[0], sgx[1]))};
+            warp_sum(sums);
+            if (lane == 0) {
+                red[buf][0][warp] = sums[0];
+                red[buf][1][warp] = sums[1];
+            }
+            __syncthreads();
+            cta_sum(red[buf], ng, lane, sums);
+            const float mg = sums[0] * invD, mgx = sums[1] * invD;
+            const f2r nmgx = p_splat(-mgx), nmgr = p_splat(-mg * rs[0]);
+            char* dxr = dxb + row * row_bytes;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                if (!ok[k]) continue;
+                f2r xh[PV], fd[PV], o[PV];
+                IO::unpackp(lds128(xs + (uint32_t)k * vk), xh);
+                IO::unpackp(lds128(xs + vrow + (uint32_t)k * vk), fd);
+#pragma unroll
+                for (int p = 0; p < PV; ++p) {
+                    xh[p] = p_mul(p_sub(xh[p], mu2), rs2);
+                    o[p] = p_fma(p_fma(xh[p], nmgx, p_mul(fd[p], sc1[k][p])), rs2, nmgr);
+                }
+                st_vec(dxr + colb[k], IO::packp(o));
+            }
+            buf ^= 1;
+        } else if (cur_ok) {  // uniform across the CTA
             // xhat = (x - mean) * rstd, g = dy * (1 + scale); row sums of g and g*xhat;
             // column sums of dy and dy*xhat. Rows past nr and idle lanes load dy = 0, so they
             // add nothing anywhere.
@@ -259,7 +313,9 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) bwd_kernel(const B
             buf ^= 1;
         }
         if constexpr (RING) {
-            if (!cur_ok) __syncthreads();  // a skipped round still fences the slot's readers
+            // A skipped round, and a wide row read again after its barrier, still fence the
+            // slot's readers before the slot is refilled.
+            if (REREAD || !cur_ok) __syncthreads();
             if (++slot == ns) {
                 slot = 0;
                 ++lap;
