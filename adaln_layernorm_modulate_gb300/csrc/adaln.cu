@@ -69,6 +69,9 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward, bool copy_ring) {
     // then warp shuffles and its barriers cover one warp, so the rows of different warps
     // never wait for each other (bf16 D=1536: 33 us against 36 us for 3 x 64 threads).
     if (forward && V % 32 == 0 && V / 32 <= 6 && V / 32 != 5) return RowCfg{(int)(V / 32), 32, true};
+    // The same for backward rows of at most 3 vectors a lane (bf16 D=768: 221 us against 236 us
+    // for 1 x 96 threads; 6 vectors a lane measured much slower: the backward keeps more).
+    if (!forward && V % 32 == 0 && V / 32 <= 3) return RowCfg{(int)(V / 32), 32, true};
     // Elements a thread: the backward keeps x, dy and two column accumulators per element,
     // the forward one value (bf16 forwards take 48, the others 32).
     int64_t target = (forward ? (bf16 ? 48 : 32) : 16) / VE;

@@ -91,6 +91,8 @@ SMALL = {
                                                         [0, 2, 1, 3], 4, x_mode=synth.ROWS_ADVERSARIAL,
                                                         mod_std=0.5, dy_std=0.02),
     "dense-bf16-d8": lambda: synth.dense("c", 107, synth.BF16, 3, 50, 8),
+    "dense-bf16-2x200x768": lambda: synth.dense("c", 118, synth.BF16, 2, 200, 768,
+                                                x_mode=synth.ROWS_SCALED, dy_std=0.02),
     "packed-bf16-d264": lambda: synth.make("c", 108, synth.BF16, 264, [5, 90, 33], [1, 1, 0], 2),
     "dense-bf16-d16384": lambda: synth.dense("c", 109, synth.BF16, 1, 40, 16384, dy_std=0.1),
     "dense-f32-d8192": lambda: synth.dense("c", 110, synth.F32, 1, 33, 8192),
