@@ -30,7 +30,8 @@ EXPORTS = (
     "adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd", "adaln_bwd_partials", "adaln_bwd_reduce",
     "adaln_fwd_varlen_workspace_size", "adaln_fwd_varlen", "adaln_bwd_varlen_workspace_size",
     "adaln_bwd_varlen", "adaln_bwd_varlen_partials", "adaln_bwd_varlen_reduce",
-    "adaln_read_status", "adaln_bwd_noalloc", "adaln_bucket_batch", "adaln_bucket_batch_real",
+    "adaln_read_status", "adaln_bwd_recompute_workspace_size", "adaln_bwd_recompute",
+    "adaln_bwd_varlen_recompute_workspace_size", "adaln_bwd_varlen_recompute", "adaln_bwd_noalloc", "adaln_bucket_batch", "adaln_bucket_batch_real",
     "adaln_fit_step_cost", "adaln_bucket_load_cv", "adaln_status_string",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ADALN_NOALLOC_SCRATCH_BYTES
@@ -67,6 +68,11 @@ def _load() -> ctypes.CDLL:
         "adaln_bwd_varlen_reduce": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64,
                                      vp, sz, ci, vp], ci),
         "adaln_read_status": ([vp, vp], ci),
+        "adaln_bwd_recompute_workspace_size": ([i64, i64, i64, ci], sz),
+        "adaln_bwd_recompute": ([vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, i64, f32, ci, vp], ci),
+        "adaln_bwd_varlen_recompute_workspace_size": ([i64, i32, i64, i64, ci], sz),
+        "adaln_bwd_varlen_recompute": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, f32, vp,
+                                        sz, ci, vp], ci),
         "adaln_bwd_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp], ci),
         "adaln_bucket_batch": ([i64, i64, i64, i32], i64),
         "adaln_bucket_batch_real": ([i64, i64, i64, ctypes.c_double], i64),
@@ -204,6 +210,30 @@ def adaln_bwd_varlen_reduce(dy, x, mean, rstd, scale, dx, dshift, dscale, cu_seq
         _ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale), _ptr(dx), _ptr(dshift),
         _ptr(dscale), _ptr(cu_seqlens), _ptr(mod_idx), nseg, total_tokens, nmod, D,
         _ptr(workspace), workspace_bytes, _dtype(dtype, dy), _stream(stream)))
+
+
+def adaln_bwd_recompute_workspace_size(Bt, N, D, dtype) -> int:
+    return int(lib().adaln_bwd_recompute_workspace_size(Bt, N, D, int(dtype)))
+
+
+def adaln_bwd_recompute(dy, x, scale, dx, dshift, dscale, workspace, workspace_bytes, Bt, N, D,
+                        eps=1e-6, dtype=None, stream=None):
+    _check("adaln_bwd_recompute", lib().adaln_bwd_recompute(
+        _ptr(dy), _ptr(x), _ptr(scale), _ptr(dx), _ptr(dshift), _ptr(dscale), _ptr(workspace),
+        workspace_bytes, Bt, N, D, eps, _dtype(dtype, x), _stream(stream)))
+
+
+def adaln_bwd_varlen_recompute_workspace_size(total_tokens, nseg, nmod, D, dtype) -> int:
+    return int(lib().adaln_bwd_varlen_recompute_workspace_size(total_tokens, nseg, nmod, D, int(dtype)))
+
+
+def adaln_bwd_varlen_recompute(dy, x, scale, dx, dshift, dscale, cu_seqlens, mod_idx, nseg,
+                               total_tokens, nmod, D, eps, workspace, workspace_bytes, dtype=None,
+                               stream=None):
+    _check("adaln_bwd_varlen_recompute", lib().adaln_bwd_varlen_recompute(
+        _ptr(dy), _ptr(x), _ptr(scale), _ptr(dx), _ptr(dshift), _ptr(dscale), _ptr(cu_seqlens),
+        _ptr(mod_idx), nseg, total_tokens, nmod, D, eps, _ptr(workspace), workspace_bytes,
+        _dtype(dtype, x), _stream(stream)))
 
 
 def adaln_read_status(workspace, stream=None) -> int:

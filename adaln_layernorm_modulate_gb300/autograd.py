@@ -8,7 +8,10 @@ Dense input: x [Bt, N, D], shift and scale [Bt, D]; token (b, n) uses row b.
 Packed input: x [R, D] with ``cu_seqlens`` [nseg + 1] and ``mod_idx`` [nseg] (int32, on the
 device); segment s uses row ``mod_idx[s]`` of shift and scale [nmod, D].
 
-The node saves x, scale and the fp32 row statistics (8 bytes a row), not y or xhat. Every
+The node saves x, scale and the fp32 row statistics (8 bytes a row), not y or xhat; with
+``save_stats=False`` it keeps no statistics (the forward's are dropped with its outputs) and
+the backward recomputes them from x (one more read of x, bitwise the same statistics and
+gradients). Every
 step runs in the library's kernels; this module only allocates outputs and workspaces
 through PyTorch's allocator and passes pointers. dshift and dscale come out of the
 library in fp32; autograd wants gradients in the parameters' dtype, so they are rounded
@@ -20,9 +23,11 @@ from typing import Optional
 
 import torch
 
-from . import (ADALN_BF16, ADALN_F32, adaln_bwd, adaln_bwd_varlen, adaln_bwd_varlen_workspace_size,
+from . import (ADALN_BF16, ADALN_F32, AdalnError, adaln_bwd, adaln_bwd_recompute,
+               adaln_bwd_recompute_workspace_size, adaln_bwd_varlen, adaln_bwd_varlen_recompute,
+               adaln_bwd_varlen_recompute_workspace_size, adaln_bwd_varlen_workspace_size,
                adaln_bwd_workspace_size, adaln_fwd, adaln_fwd_varlen, adaln_fwd_varlen_workspace_size,
-               adaln_read_status, AdalnError)
+               adaln_read_status)
 
 __all__ = ["AdaLNModulateFunction", "AdaLNModulate", "adaln_modulate"]
 
@@ -52,11 +57,12 @@ class AdaLNModulateFunction(torch.autograd.Function):
     """y = LayerNorm(x) * (1 + scale) + shift with saved fp32 mean/rstd.
 
     ``check_tables`` reads the packed call's device status after each launch (it
-    synchronises the stream): set it while validating new ``cu_seqlens``/``mod_idx``."""
+    synchronises the stream): set it while validating new ``cu_seqlens``/``mod_idx``.
+    ``save_stats=False``: keep no statistics; the backward recomputes them from x."""
 
     @staticmethod
     def forward(ctx, x, shift, scale, cu_seqlens=None, mod_idx=None, eps: float = 1e-6,
-                check_tables: bool = False):
+                check_tables: bool = False, save_stats: bool = True):
         if not x.is_cuda:
             raise ValueError("AdaLN-Modulate runs on CUDA tensors")
         x = x.contiguous()
@@ -81,7 +87,8 @@ class AdaLNModulateFunction(torch.autograd.Function):
             adaln_fwd_varlen(x, shift, scale, y, mean, rstd, cu, mod, nseg, R, nmod, D, eps, ws, nb, dt)
             if check_tables:
                 _check_status(ws, "adaln_fwd_varlen")
-            ctx.save_for_backward(x, scale, mean, rstd, cu, mod)
+            kept = (mean, rstd) if save_stats else (mean[:0], rstd[:0])
+            ctx.save_for_backward(x, scale, *kept, cu, mod)
         else:
             if x.dim() != 3 or shift.shape != (x.shape[0], D) or scale.shape != (x.shape[0], D):
                 raise ValueError("dense input: x [Bt, N, D], shift and scale [Bt, D]")
@@ -89,9 +96,12 @@ class AdaLNModulateFunction(torch.autograd.Function):
             mean = torch.empty((Bt, N), dtype=torch.float32, device=x.device)
             rstd = torch.empty((Bt, N), dtype=torch.float32, device=x.device)
             adaln_fwd(x, shift, scale, y, mean, rstd, Bt, N, D, eps, dt)
-            ctx.save_for_backward(x, scale, mean, rstd)
+            kept = (mean, rstd) if save_stats else (mean[:0], rstd[:0])
+            ctx.save_for_backward(x, scale, *kept)
         ctx.packed = packed
         ctx.check_tables = check_tables
+        ctx.save_stats = save_stats
+        ctx.eps = eps
         ctx.shift_dtype = shift.dtype
         ctx.mark_non_differentiable(mean, rstd)
         return y, mean, rstd
@@ -109,25 +119,37 @@ class AdaLNModulateFunction(torch.autograd.Function):
         if ctx.packed:
             cu, mod = ctx.saved_tensors[4:]
             R, nseg = x.shape[0], mod.numel()
-            nb = adaln_bwd_varlen_workspace_size(R, nseg, nmod, D, dt)
-            ws = _workspace(nb, x.device)
-            adaln_bwd_varlen(dy, x, mean, rstd, scale, dx, dshift, dscale, cu, mod, nseg, R, nmod, D,
-                             ws, nb, dt)
+            if ctx.save_stats:
+                nb = adaln_bwd_varlen_workspace_size(R, nseg, nmod, D, dt)
+                ws = _workspace(nb, x.device)
+                adaln_bwd_varlen(dy, x, mean, rstd, scale, dx, dshift, dscale, cu, mod, nseg, R, nmod,
+                                 D, ws, nb, dt)
+            else:
+                nb = adaln_bwd_varlen_recompute_workspace_size(R, nseg, nmod, D, dt)
+                ws = _workspace(nb, x.device)
+                adaln_bwd_varlen_recompute(dy, x, scale, dx, dshift, dscale, cu, mod, nseg, R, nmod, D,
+                                           ctx.eps, ws, nb, dt)
             if ctx.check_tables:
                 _check_status(ws, "adaln_bwd_varlen")
         else:
             Bt, N = x.shape[0], x.shape[1]
-            nb = adaln_bwd_workspace_size(Bt, N, D, dt)
-            ws = _workspace(nb, x.device)
-            adaln_bwd(dy, x, mean, rstd, scale, dx, dshift, dscale, ws, nb, Bt, N, D, dt)
-        return (dx, dshift.to(ctx.shift_dtype), dscale.to(ctx.shift_dtype), None, None, None, None)
+            if ctx.save_stats:
+                nb = adaln_bwd_workspace_size(Bt, N, D, dt)
+                ws = _workspace(nb, x.device)
+                adaln_bwd(dy, x, mean, rstd, scale, dx, dshift, dscale, ws, nb, Bt, N, D, dt)
+            else:
+                nb = adaln_bwd_recompute_workspace_size(Bt, N, D, dt)
+                ws = _workspace(nb, x.device)
+                adaln_bwd_recompute(dy, x, scale, dx, dshift, dscale, ws, nb, Bt, N, D, ctx.eps, dt)
+        return (dx, dshift.to(ctx.shift_dtype), dscale.to(ctx.shift_dtype), None, None, None, None, None)
 
 
 def adaln_modulate(x: torch.Tensor, shift: torch.Tensor, scale: torch.Tensor,
                    cu_seqlens: Optional[torch.Tensor] = None, mod_idx: Optional[torch.Tensor] = None,
-                   eps: float = 1e-6, check_tables: bool = False) -> torch.Tensor:
+                   eps: float = 1e-6, check_tables: bool = False, save_stats: bool = True) -> torch.Tensor:
     """Differentiable fused AdaLN-Modulate; returns y (the statistics stay in the graph)."""
-    y, _, _ = AdaLNModulateFunction.apply(x, shift, scale, cu_seqlens, mod_idx, eps, check_tables)
+    y, _, _ = AdaLNModulateFunction.apply(x, shift, scale, cu_seqlens, mod_idx, eps, check_tables,
+                                          save_stats)
     return y
 
 
@@ -135,12 +157,13 @@ class AdaLNModulate(torch.nn.Module):
     """Module form: ``AdaLNModulate(eps)(x, shift, scale[, cu_seqlens, mod_idx])``. It has no
     parameters of its own: shift and scale come from the conditioning branch."""
 
-    def __init__(self, eps: float = 1e-6):
+    def __init__(self, eps: float = 1e-6, save_stats: bool = True):
         super().__init__()
         self.eps = float(eps)
+        self.save_stats = bool(save_stats)
 
     def forward(self, x, shift, scale, cu_seqlens=None, mod_idx=None):
-        return adaln_modulate(x, shift, scale, cu_seqlens, mod_idx, self.eps)
+        return adaln_modulate(x, shift, scale, cu_seqlens, mod_idx, self.eps, save_stats=self.save_stats)
 
     def extra_repr(self) -> str:
-        return "eps=%g" % self.eps
+        return "eps=%g, save_stats=%s" % (self.eps, self.save_stats)

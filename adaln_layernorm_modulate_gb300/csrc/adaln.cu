@@ -551,6 +551,105 @@ const char* adaln_status_string(int status) {
 
 }  // extern "C"
 
+// ---- Backward without saved statistics ---------------------------------------------------
+// The statistics are recomputed by stats_kernel (csrc/fwd.cu) with the forward's row mapping
+// and arithmetic, so bitwise the statistics the forward computed, into a region after the
+// backward's own workspace; then the backward runs as usual.
+
+namespace {
+
+size_t recompute_stats_offset(int64_t G, int64_t nseg, int64_t D) {
+    return (bwd_need(G, nseg, D) + 255) / 256 * 256;
+}
+
+size_t bwd_recompute_workspace(int64_t R, int64_t nseg, int64_t D, bool varlen, adaln_dtype dtype) {
+    const int64_t G = bwd_tiles(R, D, varlen, dtype);
+    if (G < 0) return 0;
+    return recompute_stats_offset(G, nseg, D) + (size_t)R * 2 * sizeof(float);
+}
+
+int bwd_recompute(const void* dy, const void* x, const void* scale, void* dx, float* dshift,
+                  float* dscale, const Segments& seg, int64_t D, float eps, void* ws, size_t ws_bytes,
+                  bool varlen, adaln_dtype dtype, cudaStream_t stream) {
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return ADALN_ERR_INVALID_ARG;
+    if (int rc = check_workspace(ws, ws_bytes, kPartialsOffset)) return rc;
+    const int64_t G = bwd_tiles(seg.R, D, varlen, dtype);
+    if (G < 0) return ADALN_ERR_CUDA;
+    const size_t off = recompute_stats_offset(G, seg.nseg, D);
+    if (int rc = check_workspace(ws, ws_bytes, off + (size_t)seg.R * 2 * sizeof(float))) return rc;
+    float* mean = reinterpret_cast<float*>(static_cast<char*>(ws) + off);
+    float* rstd = mean + seg.R;
+    if (seg.R > 0) {
+        Plan f;  // the forward's row mapping for these rows
+        if (!make_plan(kFwd, dtype, D, varlen, seg.R, &f)) return ADALN_ERR_CUDA;
+        if (int rc = launched(launch_stats(x, mean, rstd, seg.R, D, eps, (int)dtype, f.c.nv, f.c.tpb,
+                                           std::min<int64_t>(f.G, seg.R), stream)))
+            return rc;
+    }
+    return run_bwd(dy, x, mean, rstd, scale, dx, dshift, dscale, seg, D, ws, ws_bytes, varlen, dtype,
+                   stream, kBoth);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t adaln_bwd_recompute_workspace_size(int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype) {
+    if (check_shape(D, dtype) || Bt < 0 || N < 0) return 0;
+    if (N > 0 && Bt > INT64_MAX / N) return 0;
+    return bwd_recompute_workspace(Bt * N, Bt, D, false, dtype);
+}
+
+int adaln_bwd_recompute(const void* dy, const void* x, const void* scale, void* dx, float* dshift,
+                        float* dscale, void* workspace, size_t workspace_bytes, int64_t Bt, int64_t N,
+                        int64_t D, float eps, adaln_dtype dtype, cudaStream_t stream) {
+    if (int rc = check_shape(D, dtype)) return rc;
+    if (Bt < 0 || N < 0) return ADALN_ERR_INVALID_ARG;
+    if (N > 0 && Bt > INT64_MAX / N) return ADALN_ERR_INVALID_ARG;
+    const int64_t R = Bt * N;
+    if (!rows_fit(R, D)) return ADALN_ERR_INVALID_ARG;
+    if (Bt == 0) return ADALN_OK;
+    if (int rc = check_io({dshift, dscale}, {})) return rc;
+    if (R > 0) {
+        if (int rc = check_io({dy, x, scale, dx}, {})) return rc;
+    }
+    return bwd_recompute(dy, x, scale, dx, dshift, dscale, dense_segments(Bt, N), D, eps, workspace,
+                         workspace_bytes, false, dtype, stream);
+}
+
+size_t adaln_bwd_varlen_recompute_workspace_size(int64_t total_tokens, int32_t nseg, int64_t nmod,
+                                                 int64_t D, adaln_dtype dtype) {
+    if (check_shape(D, dtype) || total_tokens < 0 || nseg < 0 || nmod < 0) return 0;
+    return bwd_recompute_workspace(total_tokens, nseg, D, true, dtype);
+}
+
+int adaln_bwd_varlen_recompute(const void* dy, const void* x, const void* scale, void* dx,
+                               float* dshift, float* dscale, const int32_t* cu_seqlens,
+                               const int32_t* mod_idx, int32_t nseg, int64_t total_tokens, int64_t nmod,
+                               int64_t D, float eps, void* workspace, size_t workspace_bytes,
+                               adaln_dtype dtype, cudaStream_t stream) {
+    if (int rc = check_shape(D, dtype)) return rc;
+    if (nseg < 0 || total_tokens < 0 || total_tokens > INT32_MAX || nmod < 0)
+        return ADALN_ERR_INVALID_ARG;
+    if (!rows_fit(total_tokens, D) || !rows_fit(nmod, D)) return ADALN_ERR_INVALID_ARG;
+    if (!cu_seqlens || (nseg > 0 && !mod_idx)) return ADALN_ERR_INVALID_ARG;
+    if (nseg == 0 && total_tokens > 0) return ADALN_ERR_INVALID_ARG;
+    if (nmod > 0) {
+        if (int rc = check_io({dshift, dscale}, {})) return rc;
+    }
+    if (total_tokens > 0) {
+        if (int rc = check_io({dy, x, dx}, {})) return rc;
+        if (nmod > 0) {
+            if (int rc = check_io({scale}, {})) return rc;
+        }
+    }
+    return bwd_recompute(dy, x, scale, dx, dshift, dscale,
+                         packed_segments(cu_seqlens, mod_idx, nseg, total_tokens, nmod), D, eps,
+                         workspace, workspace_bytes, true, dtype, stream);
+}
+
+}  // extern "C"
+
 // ---- dense backward without a caller workspace ---------------------------------------------
 //
 // Some callers cannot allocate device memory at the point where they run the backward: a

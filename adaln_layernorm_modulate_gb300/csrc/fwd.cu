@@ -361,4 +361,130 @@ cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, int 
     return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream);
 }
 
+// Row statistics alone, for a backward whose forward kept no statistics: the forward's row
+// mapping (NV, blockDim) and its passes 1 and 2 verbatim (shifted sum, centred sum of
+// squares, the same warp and CTA reductions), so every row gets bitwise the mean and rstd
+// the forward computed. Rows are independent here: CTA b takes rows b*R/G ... in rounds of
+// RB consecutive rows, loaded straight into registers.
+template <typename T, int NV>
+__global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) stats_kernel(const void* x, float* mean,
+                                                                         float* rstd, int64_t R, int64_t D,
+                                                                         float eps) {
+    using IO = Io<T>;
+    constexpr int VE = IO::VE;
+    constexpr int PV = VE / 2;
+    constexpr int RB = RowShape<NV>::kFwdRows;
+    __shared__ __align__(16) float red1[RB][32];
+    __shared__ __align__(16) float red2[RB][32];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int TPB = blockDim.x;
+    const int nwarps = TPB >> 5;
+    int ng = 1;
+    while (ng < nwarps) ng <<= 1;
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    const int64_t V = D / VE;
+    const int64_t r0 = tile_begin(b, R, G), r1 = tile_begin(b + 1, R, G);
+    const char* __restrict__ xb = static_cast<const char*>(x);
+    const int64_t row_bytes = D * (int64_t)sizeof(T);
+    const float invD = 1.0f / (float)D;
+    zero_absent_warps<RB>(red1, nwarps);
+    zero_absent_warps<RB>(red2, nwarps);
+    uint32_t colb[NV];
+    bool ok[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int64_t v = tid + (int64_t)k * TPB;
+        ok[k] = v < V;
+        colb[k] = (uint32_t)(v * 16);
+    }
+    __syncthreads();
+    for (int64_t row = r0; row < r1; row += RB) {
+        const int nr = (int)min((int64_t)RB, r1 - row);
+        f2r d[RB][NV][PV];
+        float K[RB], s1[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            const char* src = xb + (row + i) * row_bytes;
+            K[i] = i < nr ? IO::first(src) : 0.0f;
+            const f2r kk = p_splat(K[i]);
+            f2r acc0 = kPairZero, acc1 = kPairZero;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                IO::unpackp((i < nr && ok[k]) ? ld_stream(src + colb[k]) : make_uint4(0, 0, 0, 0), d[i][k]);
+#pragma unroll
+                for (int p = 0; p < PV; ++p) {
+                    d[i][k][p] = p_sub(d[i][k][p], kk);
+                    if (!ok[k]) d[i][k][p] = kPairZero;
+                    if (p & 1) acc1 = p_add(acc1, d[i][k][p]);
+                    else acc0 = p_add(acc0, d[i][k][p]);
+                }
+            }
+            s1[i] = p_hsum(p_add(acc0, acc1));
+        }
+        warp_sum(s1);
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < RB; ++i) red1[i][warp] = s1[i];
+        }
+        __syncthreads();
+        cta_sum(red1, ng, lane, s1);
+        float s2[RB], md[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            md[i] = s1[i] * invD;
+            const f2r pm = p_splat(md[i]);
+            f2r acc0 = kPairZero, acc1 = kPairZero;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+#pragma unroll
+                for (int p = 0; p < PV; ++p) {
+                    d[i][k][p] = p_sub(d[i][k][p], pm);
+                    if (!ok[k]) d[i][k][p] = kPairZero;
+                    if (p & 1) acc1 = p_fma(d[i][k][p], d[i][k][p], acc1);
+                    else acc0 = p_fma(d[i][k][p], d[i][k][p], acc0);
+                }
+            }
+            s2[i] = p_hsum(p_add(acc0, acc1));
+        }
+        warp_sum(s2);
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < RB; ++i) red2[i][warp] = s2[i];
+        }
+        __syncthreads();
+        cta_sum(red2, ng, lane, s2);
+        if (tid == 0) {
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                if (i < nr) {
+                    mean[row + i] = K[i] + md[i];
+                    rstd[row + i] = rsqrtf(s2[i] * invD + eps);
+                }
+            }
+        }
+    }
+}
+
+template <typename T>
+static const void* pick_stats(int nv) {
+    switch (nv) {
+        case 1: return reinterpret_cast<const void*>(&stats_kernel<T, 1>);
+        case 2: return reinterpret_cast<const void*>(&stats_kernel<T, 2>);
+        case 3: return reinterpret_cast<const void*>(&stats_kernel<T, 3>);
+        case 4: return reinterpret_cast<const void*>(&stats_kernel<T, 4>);
+        case 6: return reinterpret_cast<const void*>(&stats_kernel<T, 6>);
+        case 8: return reinterpret_cast<const void*>(&stats_kernel<T, 8>);
+        default: return nullptr;
+    }
+}
+
+cudaError_t launch_stats(const void* x, float* mean, float* rstd, int64_t R, int64_t D, float eps,
+                         int dtype, int nv, int tpb, int64_t G, cudaStream_t stream) {
+    const void* fn = dtype == 0 ? pick_stats<float>(nv) : dtype == 1 ? pick_stats<__nv_bfloat16>(nv) : nullptr;
+    if (!fn || G < 1) return cudaErrorInvalidValue;
+    void* params[] = {&x, &mean, &rstd, &R, &D, &eps};
+    return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, 0, stream);
+}
+
 }  // namespace adaln

@@ -15,6 +15,11 @@ cudaError_t fwd_blocks_per_sm(int dtype, int nv, bool varlen, int ring, bool ful
 cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, int ring, bool full,
                        int64_t G, int tpb, size_t smem, cudaStream_t stream);
 
+// Row statistics alone (mean, rstd of R rows of x), with the forward's mapping (nv, tpb)
+// and arithmetic; G CTAs, plain loads.
+cudaError_t launch_stats(const void* x, float* mean, float* rstd, int64_t R, int64_t D, float eps,
+                         int dtype, int nv, int tpb, int64_t G, cudaStream_t stream);
+
 cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
                               size_t smem, int* out);
 cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,

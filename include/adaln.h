@@ -151,6 +151,25 @@ int adaln_bwd_varlen_reduce(const void* dy, const void* x, const float* mean, co
                             int64_t total_tokens, int64_t nmod, int64_t D, void* workspace,
                             size_t workspace_bytes, adaln_dtype dtype, cudaStream_t stream);
 
+/* Backward without saved statistics, for callers that do not keep the forward's mean and
+ * rstd (8 bytes a row of activation memory): they are first recomputed from x with the
+ * forward's row mapping and arithmetic (bitwise the values the forward wrote, for the same
+ * eps), into the end of the workspace, then the backward runs as adaln_bwd /
+ * adaln_bwd_varlen. It costs one more read of x.
+ * The workspace must hold the *_recompute_workspace_size bytes (which include the
+ * backward's own); arguments and errors otherwise as adaln_bwd / adaln_bwd_varlen. */
+size_t adaln_bwd_recompute_workspace_size(int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype);
+int adaln_bwd_recompute(const void* dy, const void* x, const void* scale, void* dx, float* dshift,
+                        float* dscale, void* workspace, size_t workspace_bytes, int64_t Bt, int64_t N,
+                        int64_t D, float eps, adaln_dtype dtype, cudaStream_t stream);
+size_t adaln_bwd_varlen_recompute_workspace_size(int64_t total_tokens, int32_t nseg, int64_t nmod,
+                                                 int64_t D, adaln_dtype dtype);
+int adaln_bwd_varlen_recompute(const void* dy, const void* x, const void* scale, void* dx,
+                               float* dshift, float* dscale, const int32_t* cu_seqlens,
+                               const int32_t* mod_idx, int32_t nseg, int64_t total_tokens, int64_t nmod,
+                               int64_t D, float eps, void* workspace, size_t workspace_bytes,
+                               adaln_dtype dtype, cudaStream_t stream);
+
 /* Synchronises `stream`, then returns the device-side status recorded in `workspace` by
  * the last packed forward/backward (or backward) that used it: ADALN_OK,
  * ADALN_ERR_BAD_SEQLENS, ADALN_ERR_BAD_MOD_IDX or ADALN_ERR_TIMEOUT, in that order of

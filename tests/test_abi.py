@@ -77,6 +77,9 @@ def test_argument_checks_before_any_device_work():
     assert L.adaln_fwd(16, 16, 16, 16, 16, 16, -1, 1, 64, 1e-6, 1, None) == 1
     # empty problems are valid no-ops
     assert L.adaln_fwd(None, None, None, None, None, None, 0, 5, 64, 1e-6, 1, None) == 0
+    # backward recomputing the statistics: eps, workspace
+    assert L.adaln_bwd_recompute(16, 16, 16, 16, 16, 16, 256, 1 << 20, 1, 1, 64, 0.0, 1, None) == 1
+    assert L.adaln_bwd_recompute(16, 16, 16, 16, 16, 16, None, 1 << 20, 1, 1, 64, 1e-6, 1, None) == 4
     # null and misaligned pointers
     assert L.adaln_fwd(None, 16, 16, 16, 16, 16, 1, 1, 64, 1e-6, 1, None) == 1
     assert L.adaln_fwd(24, 16, 16, 16, 16, 16, 1, 1, 64, 1e-6, 1, None) == 3

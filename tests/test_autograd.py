@@ -12,7 +12,7 @@ def test_cpu_tensors_are_refused():
 
     from adaln_layernorm_modulate_gb300.autograd import AdaLNModulate
     m = AdaLNModulate(1e-6)
-    assert "eps=1e-06" in repr(m)
+    assert "eps=1e-06, save_stats=True" in repr(m)
     x = torch.zeros(1, 4, 64)
     with pytest.raises(ValueError):
         m(x, torch.zeros(1, 64), torch.zeros(1, 64))
@@ -26,8 +26,9 @@ CASES = {
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("save_stats", [True, False], ids=["saved-stats", "recomputed-stats"])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_autograd_matches_direct_calls_and_oracle(orc, name):
+def test_autograd_matches_direct_calls_and_oracle(orc, name, save_stats):
     import torch
 
     import adaln_layernorm_modulate_gb300 as A
@@ -43,9 +44,9 @@ def test_autograd_matches_direct_calls_and_oracle(orc, name):
     scale = d.scale.clone().requires_grad_(True)
     dy = d.dy if packed else d.dy.view(w.dense[0], w.dense[1], w.D)
     if packed:
-        y = adaln_modulate(x, shift, scale, d.cu, d.mod, eps=H.EPS, check_tables=True)
+        y = adaln_modulate(x, shift, scale, d.cu, d.mod, eps=H.EPS, check_tables=True, save_stats=save_stats)
     else:
-        y = adaln_modulate(x, shift, scale, eps=H.EPS)
+        y = adaln_modulate(x, shift, scale, eps=H.EPS, save_stats=save_stats)
     y.backward(dy)
 
     # Same kernels as the C-ABI path: bitwise equal.

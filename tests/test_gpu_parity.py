@@ -367,3 +367,34 @@ def test_outputs_stay_inside_their_buffers():
     for buf, n in ((yb, w.R * w.D), (mb, w.R), (rb, w.R), (dxb, w.R * w.D), (shb, w.nmod * w.D),
                    (scb, w.nmod * w.D)):
         assert intact(buf, n)
+
+
+@pytest.mark.parametrize("name", ["dense-bf16-2x300x1536", "packed-bf16-d3072-ragged",
+                                  "packed-f32-d3072-adversarial", "dense-bf16-d16384",
+                                  "packed-bf16-d8-long-tiles"])
+def test_recomputed_statistics_are_bitwise_the_saved_ones(name):
+    """A backward that recomputes mean/rstd from x gives bitwise the dx, dshift and dscale of
+    the backward that reads the forward's saved statistics."""
+    import adaln_layernorm_modulate_gb300 as A
+    t = H.torch()
+    w = SMALL[name]()
+    d = H.upload(w)
+    y, mean, rstd, _ = H.gpu_fwd(d)
+    dx, dsh, dsc, _ = H.gpu_bwd(d, mean, rstd)
+    dx2 = t.empty_like(dx)
+    dsh2, dsc2 = t.empty_like(dsh), t.empty_like(dsc)
+    if w.dense is None:
+        nb = A.adaln_bwd_varlen_recompute_workspace_size(w.R, w.nseg, w.nmod, w.D, w.dtype)
+        ws = t.empty(nb, dtype=t.uint8, device="cuda")
+        A.adaln_bwd_varlen_recompute(d.dy, d.x, d.scale, dx2, dsh2, dsc2, d.cu, d.mod, w.nseg, w.R,
+                                     w.nmod, w.D, H.EPS, ws, nb, w.dtype)
+        assert A.adaln_read_status(ws) == 0
+    else:
+        Bt, N = w.dense
+        nb = A.adaln_bwd_recompute_workspace_size(Bt, N, w.D, w.dtype)
+        assert nb > A.adaln_bwd_workspace_size(Bt, N, w.D, w.dtype)
+        ws = t.empty(nb, dtype=t.uint8, device="cuda")
+        A.adaln_bwd_recompute(d.dy, d.x, d.scale, dx2, dsh2, dsc2, ws, nb, Bt, N, w.D, H.EPS, w.dtype)
+    t.cuda.synchronize()
+    assert t.equal(dx, dx2)
+    assert t.equal(dsh, dsh2) and t.equal(dsc, dsc2)
