@@ -39,10 +39,9 @@ int current_sms(int* dev_out) {
 // How a row of width D is spread over a CTA: each thread owns `nv` 16-byte vectors
 // (v = tid + k * tpb), so a CTA holds one row in registers. The per-row reduction work is
 // paid once per thread per row, so more elements per thread amortise it better, until
-// registers run out: the forward holds about 32 elements a thread, the backward (which
-// keeps twice as many values per element) about 16. Narrow rows shrink nv so a warp is not
-// left idle; wide rows grow it so a row fits the CTA size the kernel is compiled for
-// (max_threads(nv, elements per vector)).
+// registers run out (row_cfg below gives the measured preferences). Narrow rows shrink nv
+// so a warp is not left idle; wide rows grow it so a row fits the CTA size the kernel is
+// compiled for (max_threads(nv, elements per vector)).
 struct RowCfg {
     int nv;
     int tpb;

@@ -14,7 +14,8 @@
 // As in the forward, the ring variant has one thread copy whole rows of x and dy into a
 // shared-memory ring with bulk (TMA) copies completing on per-slot mbarriers; the rows'
 // saved mean/rstd are loaded one round ahead into registers; the elementwise math runs on
-// fp32 pairs.
+// fp32 pairs. Wide rows (6 or more vectors a thread) are read from the ring twice, once for
+// the sums and accumulators and once for dx, instead of being held in registers.
 #include "common.cuh"
 #include "launch.h"
 
