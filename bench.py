@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import subprocess
 import sys
@@ -130,10 +131,15 @@ def hbm_peak():
 
 
 def kernel_sources_sha() -> str:
+    """Hash of the backward kernel's code (its sources with comments and blank space
+    removed): a recorded traffic figure stays valid across comment edits, not code edits."""
     h = hashlib.sha256()
     for rel in ("adaln_layernorm_modulate_gb300/csrc/bwd.cu", "adaln_layernorm_modulate_gb300/csrc/common.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 
