@@ -18,8 +18,8 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import re
 import os
+import re
 import subprocess
 import sys
 import tempfile
