@@ -103,3 +103,26 @@ def test_workspace_size_rejects_bad_shapes():
     assert A.adaln_fwd_varlen_workspace_size(10, 2, 64, 1) > 0
     assert A.adaln_bwd_workspace_size(1, 1, 7, 1) == 0
     assert A.adaln_bwd_varlen_workspace_size(-1, 1, 1, 64, 1) == 0
+
+
+def test_header_compiles_as_c_and_a_c_program_links(tmp_path):
+    """include/adaln.h is a plain C header: a C99 program includes it, links libadaln and
+    calls a host-only entry point."""
+    import shutil
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    A.lib()  # the library is built
+    src = tmp_path / "use_adaln.c"
+    src.write_text('#include "adaln.h"\n'
+                   "int main(void) {\n"
+                   "    adaln_dtype d = ADALN_BF16;\n"
+                   "    (void)d;\n"
+                   "    return adaln_bucket_batch(256, 131072, 131072LL * 4096, 2) == 512 ? 0 : 1;\n"
+                   "}\n")
+    exe = tmp_path / "use_adaln"
+    libdir = os.path.dirname(A.LIB_PATH)
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                    str(src), "-L", libdir, "-ladaln", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                   check=True, capture_output=True)
+    assert subprocess.run([str(exe)]).returncode == 0
