@@ -96,6 +96,8 @@ SMALL = {
     "packed-bf16-d264": lambda: synth.make("c", 108, synth.BF16, 264, [5, 90, 33], [1, 1, 0], 2),
     "dense-bf16-d16384": lambda: synth.dense("c", 109, synth.BF16, 1, 40, 16384, dy_std=0.1),
     "dense-f32-d8192": lambda: synth.dense("c", 110, synth.F32, 1, 33, 8192),
+    # Rows too wide for a two-round backward ring: plain loads, x and dy read twice.
+    "dense-f32-2x21x16384": lambda: synth.dense("c", 119, synth.F32, 2, 21, 16384, dy_std=0.1),
     "packed-f32-d128-many": lambda: synth.make(
         "c", 111, synth.F32, 128, list(np.random.default_rng(5).integers(0, 10, 100)),
         list(np.random.default_rng(6).integers(0, 13, 100)), 13),
