@@ -49,21 +49,27 @@ struct RowCfg {
 };
 
 
-// Row mapping of a launch. `copy_ring`: the forward will stage rows with the per-thread
-// copy ring (long tiles), otherwise with the bulk ring or plain loads. The preferences were
-// measured on GB300 (bf16 D=3072 forward: 3 x 128 threads with the copy ring, 992 us on the
-// packed workload against 1035 us for 4 x 96; 6 x 64 threads with the bulk ring, 67.9 us on
-// a 32,760-token segment against 70.6 us).
-RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward, bool copy_ring) {
+// The forward's per-thread copy ring is used with one mapping only, where it measured
+// faster than the bulk ring: bf16 rows, three vectors a thread (two rows a round), covering
+// the row with at least four warps (bf16 D=3072: 3 x 128 threads; 992 us on the packed
+// workload against 1035 us with the bulk ring, 134 us against 143 us on the MMDiT streams).
+// With fp32 rows, or any other mapping, it measured slower (MMDiT fp32: 290 us against 263).
+bool copy_ring_cfg(int64_t D, adaln_dtype dtype, RowCfg* c) {
+    if (dtype != ADALN_BF16) return false;
+    const int64_t V = D / 8;
+    if (V % 3 != 0 || (V / 3) % 32 != 0 || V / 3 < 128 || V / 3 > max_threads(3, 8)) return false;
+    *c = RowCfg{3, (int)(V / 3), true};
+    return true;
+}
+
+// Row mapping of a launch (the bulk ring, plain loads, and the backward). The preferences
+// were measured on GB300 (bf16 D=3072 forward: 6 x 64 threads, 67.9 us on a 32,760-token
+// segment against 70.6 us for 4 x 96).
+RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
     static const int kNv[] = {1, 2, 3, 4, 6, 8};
     const bool bf16 = dtype == ADALN_BF16;
     const int64_t VE = bf16 ? 8 : 4;
     const int64_t V = D / VE;
-    // Copy ring: three vectors a thread (two rows a round) when that covers the row with at
-    // least four warps.
-    if (forward && copy_ring && V % 3 == 0 && (V / 3) % 32 == 0 && V / 3 >= 128 &&
-        V / 3 <= max_threads(3, (int)VE))
-        return RowCfg{3, (int)(V / 3), true};
     // Forward rows of at most 6 vectors per lane: one warp per row. The CTA's reductions are
     // then warp shuffles and its barriers cover one warp, so the rows of different warps
     // never wait for each other (bf16 D=1536: 33 us against 36 us for 3 x 64 threads).
@@ -103,9 +109,11 @@ constexpr size_t kRingBudget = 150 * 1024;
 // Rows whose two-round ring exceeds the budget still get one, up to this size (fp32
 // D=12288 backward: two rounds of 96 KB), rather than plain loads into registers.
 constexpr size_t kRingLimit = 200 * 1024;
-// Forward tiles at least this many rows long stage rows with the per-thread copy ring,
-// shorter ones with the bulk ring (which starts faster, see fwd.cu).
-constexpr int64_t kCopyRingRows = 256;
+// Forward tiles (per resident CTA slot) at least this many rows long stage rows with the
+// per-thread copy ring where copy_ring_cfg allows it, shorter ones with the bulk ring (which
+// starts faster, see fwd.cu): 36 rows a slot measured faster with the bulk ring, 73 with
+// the copy ring.
+constexpr int64_t kCopyRingRows = 64;
 
 struct Plan {
     RowCfg c;
@@ -183,13 +191,13 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
     const int sms = current_sms(&dev);
     if (sms <= 0) return false;
     p->sms = sms;
-    p->c = row_cfg(D, dtype, kind == kFwd, false);
+    p->c = row_cfg(D, dtype, kind == kFwd);
     // A ring needs two rounds; rows too wide for two rounds in kRingLimit load into registers.
     p->ring = 2 * ring_round_bytes(kind, p->c, kRingBulk) + kRingHeader <= kRingLimit ? kRingBulk : kRingNone;
     p->full = p->ring && p->c.full;
     if (!ring_shape(kind, dtype, varlen, dev, p)) return false;
-    if (kind == kFwd && p->ring == kRingBulk && R >= kCopyRingRows * p->G) {
-        const RowCfg copy = row_cfg(D, dtype, true, true);
+    RowCfg copy;
+    if (kind == kFwd && p->ring == kRingBulk && copy_ring_cfg(D, dtype, &copy) && R >= kCopyRingRows * p->G) {
         if (2 * ring_round_bytes(kind, copy, kRingCopy) + kRingHeader <= kRingLimit) {
             p->c = copy;
             p->ring = kRingCopy;

@@ -1,6 +1,9 @@
 """The pipelined end-to-end step of bench.py (segment chunks on copy-in, compute and
-copy-out streams) gives the whole-batch results: y, dx and the statistics bitwise,
-dshift/dscale within a summation-order difference."""
+copy-out streams) gives bitwise the results of the same chunk calls made one after another
+on one stream (so no copy overtakes a launch that needs it), and the whole-batch call's
+results within rounding: a chunk's forward may map its rows differently from the whole
+batch's (tile length decides between the two forward stagings for some bf16 widths), which
+changes the summation order of the row statistics."""
 import numpy as np
 import pytest
 
@@ -41,20 +44,44 @@ def test_chunked_end_to_end_step_matches_whole_batch_calls():
     step()
     torch.cuda.synchronize()
 
-    cu = torch.from_numpy(w.cu_seqlens.astype(np.int32)).to(dev)
-    mod = torch.from_numpy(w.mod_idx.astype(np.int32)).to(dev)
+    cu = np.asarray(w.cu_seqlens)
     ref = {k: torch.empty_like(v) for k, v in outs.items()}
+    for s0, s1 in chunks:
+        t0, t1 = int(cu[s0]), int(cu[s1])
+        r, ns = t1 - t0, s1 - s0
+        lcu = torch.from_numpy((cu[s0:s1 + 1] - t0).astype(np.int32)).to(dev)
+        lmod = torch.arange(ns, dtype=torch.int32, device=dev)
+        fn = A.adaln_fwd_varlen_workspace_size(r, ns, w.D, w.dtype)
+        bn = A.adaln_bwd_varlen_workspace_size(r, ns, ns, w.D, w.dtype)
+        fws = torch.empty(fn, dtype=torch.uint8, device=dev)
+        bws = torch.empty(bn, dtype=torch.uint8, device=dev)
+        A.adaln_fwd_varlen(d["x"][t0:t1], d["shift"][s0:s1], d["scale"][s0:s1], ref["y"][t0:t1],
+                           ref["mean"][t0:t1], ref["rstd"][t0:t1], lcu, lmod, ns, r, ns, D, bench.EPS,
+                           fws, fn, w.dtype, sptr)
+        A.adaln_bwd_varlen(d["dy"][t0:t1], d["x"][t0:t1], ref["mean"][t0:t1], ref["rstd"][t0:t1],
+                           d["scale"][s0:s1], ref["dx"][t0:t1], ref["dshift"][s0:s1], ref["dscale"][s0:s1],
+                           lcu, lmod, ns, r, ns, D, bws, bn, w.dtype, sptr)
+    torch.cuda.synchronize()
+    for k in outs:
+        assert torch.equal(out_h[k], ref[k].cpu()), k
+
+    # The whole batch in one call.
+    dcu = torch.from_numpy(w.cu_seqlens.astype(np.int32)).to(dev)
+    dmod = torch.from_numpy(w.mod_idx.astype(np.int32)).to(dev)
+    whole = {k: torch.empty_like(v) for k, v in outs.items()}
     fn = A.adaln_fwd_varlen_workspace_size(R, nseg, D, w.dtype)
     bn = A.adaln_bwd_varlen_workspace_size(R, nseg, nmod, D, w.dtype)
     fws = torch.empty(fn, dtype=torch.uint8, device=dev)
     bws = torch.empty(bn, dtype=torch.uint8, device=dev)
-    A.adaln_fwd_varlen(d["x"], d["shift"], d["scale"], ref["y"], ref["mean"], ref["rstd"], cu, mod, nseg,
-                       R, nmod, D, bench.EPS, fws, fn, w.dtype, sptr)
-    A.adaln_bwd_varlen(d["dy"], d["x"], ref["mean"], ref["rstd"], d["scale"], ref["dx"], ref["dshift"],
-                       ref["dscale"], cu, mod, nseg, R, nmod, D, bws, bn, w.dtype, sptr)
+    A.adaln_fwd_varlen(d["x"], d["shift"], d["scale"], whole["y"], whole["mean"], whole["rstd"], dcu, dmod,
+                       nseg, R, nmod, D, bench.EPS, fws, fn, w.dtype, sptr)
+    A.adaln_bwd_varlen(d["dy"], d["x"], whole["mean"], whole["rstd"], d["scale"], whole["dx"],
+                       whole["dshift"], whole["dscale"], dcu, dmod, nseg, R, nmod, D, bws, bn,
+                       w.dtype, sptr)
     torch.cuda.synchronize()
-    for k in ("y", "dx", "mean", "rstd"):
-        assert torch.equal(out_h[k], ref[k].cpu()), k
-    for k in ("dshift", "dscale"):
-        a, b = out_h[k].double(), ref[k].cpu().double()
-        assert float((a - b).norm() / b.norm()) < 1e-5, k
+    for k in ("mean", "rstd"):
+        a, b = out_h[k].double(), whole[k].cpu().double()
+        assert float((a - b).abs().max() / b.abs().max()) < 1e-5, k
+    for k, tol in (("y", 4e-3), ("dx", 4e-3), ("dshift", 1e-4), ("dscale", 1e-4)):
+        a, b = out_h[k].double(), whole[k].cpu().double()
+        assert float((a - b).norm() / b.norm()) < tol, k

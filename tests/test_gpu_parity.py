@@ -107,7 +107,7 @@ SMALL = {
     "packed-f32-d64-3000seg": lambda: synth.make(
         "c", 113, synth.F32, 64, list(np.random.default_rng(7).integers(0, 10, 3000)),
         list(np.random.default_rng(8).integers(0, 40, 3000)), 41),
-    # Tiles of more than 256 rows: the forward stages rows with its per-thread copy ring.
+    # Tiles of hundreds of thousands of narrow rows: many rounds of the forward's bulk ring.
     "packed-bf16-d8-long-tiles": lambda: synth.make(
         "c", 115, synth.BF16, 8, [400000, 3, 700000], [1, 0, 1], 2,
         x_mode=synth.ROWS_SCALED, dy_std=0.02),
