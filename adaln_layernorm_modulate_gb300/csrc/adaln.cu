@@ -50,15 +50,14 @@ struct RowCfg {
 
 
 // The forward's per-thread copy ring is used with one mapping only, where it measured
-// faster than the bulk ring: bf16 rows, three vectors a thread (two rows a round), covering
-// the row with at least four warps (bf16 D=3072: 3 x 128 threads; 992 us on the packed
-// workload against 1035 us with the bulk ring, 134 us against 143 us on the MMDiT streams).
-// With fp32 rows, or any other mapping, it measured slower (MMDiT fp32: 290 us against 263).
+// faster than the bulk ring: bf16 rows of 384 vectors, three a thread over four warps (two
+// rows a round), i.e. D=3072 (992 us on the packed workload against 1035 us with the bulk
+// ring, 134 us against 143 us on the MMDiT streams). With fp32 rows or any other mapping
+// it measured slower (MMDiT fp32: 290 us against 263; bf16 D=6144, 3 x 256 threads at 143
+// rows a CTA slot: 70% of the HBM peak against 90%).
 bool copy_ring_cfg(int64_t D, adaln_dtype dtype, RowCfg* c) {
-    if (dtype != ADALN_BF16) return false;
-    const int64_t V = D / 8;
-    if (V % 3 != 0 || (V / 3) % 32 != 0 || V / 3 < 128 || V / 3 > max_threads(3, 8)) return false;
-    *c = RowCfg{3, (int)(V / 3), true};
+    if (dtype != ADALN_BF16 || D != 3 * 128 * 8) return false;
+    *c = RowCfg{3, 128, true};
     return true;
 }
 
