@@ -371,15 +371,25 @@ def test_outputs_stay_inside_their_buffers():
         assert intact(buf, n)
 
 
+# Too large for the element-by-element oracle cases, compared GPU against GPU: 90,008 bf16
+# rows of D=3072 are more than 64 rows a resident CTA slot on GB300 (912 slots), so the
+# forward stages them with its per-thread copy ring and maps them 3 x 128 threads.
+RECOMPUTE_ONLY = {
+    "packed-bf16-d3072-copy-ring": lambda: synth.make(
+        "c", 120, synth.BF16, 3072, [40000, 7, 50000, 1], [0, 1, 0, 1], 2,
+        x_mode=synth.ROWS_SCALED, dy_std=0.02),
+}
+
+
 @pytest.mark.parametrize("name", ["dense-bf16-2x300x1536", "packed-bf16-d3072-ragged",
                                   "packed-f32-d3072-adversarial", "dense-bf16-d16384",
-                                  "packed-bf16-d8-long-tiles"])
+                                  "packed-bf16-d8-long-tiles", "packed-bf16-d3072-copy-ring"])
 def test_recomputed_statistics_are_bitwise_the_saved_ones(name):
     """A backward that recomputes mean/rstd from x gives bitwise the dx, dshift and dscale of
     the backward that reads the forward's saved statistics."""
     import adaln_layernorm_modulate_gb300 as A
     t = H.torch()
-    w = SMALL[name]()
+    w = (SMALL.get(name) or RECOMPUTE_ONLY[name])()
     d = H.upload(w)
     y, mean, rstd, _ = H.gpu_fwd(d)
     dx, dsh, dsc, _ = H.gpu_bwd(d, mean, rstd)
@@ -400,3 +410,5 @@ def test_recomputed_statistics_are_bitwise_the_saved_ones(name):
     t.cuda.synchronize()
     assert t.equal(dx, dx2)
     assert t.equal(dsh, dsh2) and t.equal(dsc, dsc2)
+    del d, y, dx, dx2
+    t.cuda.empty_cache()
