@@ -108,10 +108,10 @@ constexpr size_t kRingBudget = 150 * 1024;
 // Rows whose two-round ring exceeds the budget still get one, up to this size (fp32
 // D=12288 backward: two rounds of 96 KB), rather than plain loads into registers.
 constexpr size_t kRingLimit = 200 * 1024;
-// Forward tiles (per resident CTA slot) at least this many rows long stage rows with the
-// per-thread copy ring where copy_ring_cfg allows it, shorter ones with the bulk ring (which
-// starts faster, see fwd.cu): 36 rows a slot measured faster with the bulk ring, 73 with
-// the copy ring.
+// Forwards with at least this many rows per resident CTA slot of the bulk-ring plan stage
+// rows with the per-thread copy ring where copy_ring_cfg allows it, shorter ones with the
+// bulk ring (which starts faster, see fwd.cu). bf16 D=3072 (912 bulk-ring slots on 152
+// SMs): 36 rows a slot measured faster with the bulk ring, 73 with the copy ring.
 constexpr int64_t kCopyRingRows = 64;
 
 struct Plan {
