@@ -96,6 +96,13 @@ SMALL = {
     "packed-bf16-d264": lambda: synth.make("c", 108, synth.BF16, 264, [5, 90, 33], [1, 1, 0], 2),
     "dense-bf16-d16384": lambda: synth.dense("c", 109, synth.BF16, 1, 40, 16384, dy_std=0.1),
     "dense-f32-d8192": lambda: synth.dense("c", 110, synth.F32, 1, 33, 8192),
+    # A backward ring of two rounds over the 150 KB budget (2 x 96 KB): fp32 D=12288.
+    "dense-f32-2x17x12288": lambda: synth.dense("c", 121, synth.F32, 2, 17, 12288, dy_std=0.1),
+    # bf16 rows of 8 vectors a thread over 7 warps (D=14336) and of 10240 (an exact cover
+    # away from the forward's preferred 6 vectors a thread).
+    "dense-bf16-1x37x14336": lambda: synth.dense("c", 122, synth.BF16, 1, 37, 14336, dy_std=0.1),
+    "packed-bf16-d10240": lambda: synth.make("c", 123, synth.BF16, 10240, [20, 1, 25], [0, 1, 0], 2,
+                                             x_mode=synth.ROWS_SCALED, dy_std=0.02),
     # Rows too wide for a two-round backward ring: plain loads, x and dy read twice.
     "dense-f32-2x21x16384": lambda: synth.dense("c", 119, synth.F32, 2, 21, 16384, dy_std=0.1),
     "packed-f32-d128-many": lambda: synth.make(
