@@ -31,7 +31,8 @@ EXPORTS = (
     "adaln_fwd_varlen_workspace_size", "adaln_fwd_varlen", "adaln_bwd_varlen_workspace_size",
     "adaln_bwd_varlen", "adaln_bwd_varlen_partials", "adaln_bwd_varlen_reduce",
     "adaln_read_status", "adaln_bwd_recompute_workspace_size", "adaln_bwd_recompute",
-    "adaln_bwd_varlen_recompute_workspace_size", "adaln_bwd_varlen_recompute", "adaln_bwd_noalloc", "adaln_bucket_batch", "adaln_bucket_batch_real",
+    "adaln_bwd_varlen_recompute_workspace_size", "adaln_bwd_varlen_recompute", "adaln_bwd_noalloc", "adaln_noalloc_read_status",
+    "adaln_bucket_batch", "adaln_bucket_batch_real",
     "adaln_fit_step_cost", "adaln_bucket_load_cv", "adaln_status_string",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ADALN_NOALLOC_SCRATCH_BYTES
@@ -74,6 +75,7 @@ def _load() -> ctypes.CDLL:
         "adaln_bwd_varlen_recompute": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, f32, vp,
                                         sz, ci, vp], ci),
         "adaln_bwd_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp], ci),
+        "adaln_noalloc_read_status": ([vp], ci),
         "adaln_bucket_batch": ([i64, i64, i64, i32], i64),
         "adaln_bucket_batch_real": ([i64, i64, i64, ctypes.c_double], i64),
         "adaln_fit_step_cost": ([vp, vp, vp, i64, ctypes.c_double, ctypes.c_double,
@@ -247,6 +249,10 @@ def adaln_bwd_noalloc(dy, x, mean, rstd, scale, dx, dshift, dscale, Bt, N, D, dt
     _check("adaln_bwd_noalloc", lib().adaln_bwd_noalloc(
         _ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale), _ptr(dx), _ptr(dshift),
         _ptr(dscale), Bt, N, D, _dtype(dtype, dy), _stream(stream)))
+
+
+def adaln_noalloc_read_status(stream=None) -> int:
+    return int(lib().adaln_noalloc_read_status(_stream(stream)))
 
 
 def adaln_bucket_batch(S, M_mem, M_comp, p) -> int:

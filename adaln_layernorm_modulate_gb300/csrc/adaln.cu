@@ -270,6 +270,30 @@ Segments packed_segments(const int32_t* cu, const int32_t* mod, int32_t nseg, in
     return Segments{cu, mod, nseg, 0, nmod, total};
 }
 
+// Synchronises `stream`, then ORs the per-CTA status words a kernel left in `ws` (see
+// adaln_read_status).
+int read_status_words(const void* ws, cudaStream_t stream) {
+    if (!ws) return ADALN_ERR_WORKSPACE;
+    WsHeader h{};
+    if (cudaMemcpyAsync(&h, ws, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return ADALN_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ADALN_ERR_CUDA;
+    if (h.magic != kStatusMagic || h.nwords == 0 || h.nwords > (uint32_t)kMaxCtas)
+        return ADALN_ERR_WORKSPACE;
+    std::vector<uint32_t> words(h.nwords);
+    if (cudaMemcpyAsync(words.data(), static_cast<const char*>(ws) + kHeaderBytes,
+                        sizeof(uint32_t) * words.size(), cudaMemcpyDeviceToHost,
+                        stream) != cudaSuccess)
+        return ADALN_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ADALN_ERR_CUDA;
+    uint32_t all = 0;
+    for (uint32_t w : words) all |= w;
+    if (all & kErrSeqlens) return ADALN_ERR_BAD_SEQLENS;
+    if (all & kErrModIdx) return ADALN_ERR_BAD_MOD_IDX;
+    if (all & kErrTimeout) return ADALN_ERR_TIMEOUT;
+    return ADALN_OK;
+}
+
 // ---- shared bodies of the dense and packed calls -----------------------------------------
 
 int run_fwd(const void* x, const void* shift, const void* scale, void* y, float* mean,
@@ -508,25 +532,7 @@ int adaln_bwd_varlen_reduce(const void* dy, const void* x, const float* mean, co
 }
 
 int adaln_read_status(const void* workspace, cudaStream_t stream) {
-    if (!workspace) return ADALN_ERR_WORKSPACE;
-    WsHeader h{};
-    if (cudaMemcpyAsync(&h, workspace, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        return ADALN_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return ADALN_ERR_CUDA;
-    if (h.magic != kStatusMagic || h.nwords == 0 || h.nwords > (uint32_t)kMaxCtas)
-        return ADALN_ERR_WORKSPACE;
-    std::vector<uint32_t> words(h.nwords);
-    if (cudaMemcpyAsync(words.data(), static_cast<const char*>(workspace) + kHeaderBytes,
-                        sizeof(uint32_t) * words.size(), cudaMemcpyDeviceToHost,
-                        stream) != cudaSuccess)
-        return ADALN_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return ADALN_ERR_CUDA;
-    uint32_t all = 0;
-    for (uint32_t w : words) all |= w;
-    if (all & kErrSeqlens) return ADALN_ERR_BAD_SEQLENS;
-    if (all & kErrModIdx) return ADALN_ERR_BAD_MOD_IDX;
-    if (all & kErrTimeout) return ADALN_ERR_TIMEOUT;
-    return ADALN_OK;
+    return read_status_words(workspace, stream);
 }
 
 int64_t adaln_bucket_batch(int64_t S, int64_t M_mem, int64_t M_comp, int32_t p) {
@@ -706,4 +712,12 @@ extern "C" int adaln_bwd_noalloc(const void* dy, const void* x, const float* mea
     // needs more scratch than the fixed array holds.
     return bwd_dense(dy, x, mean, rstd, scale, dx, dshift, dscale, scratch,
                      (size_t)ADALN_NOALLOC_SCRATCH_BYTES, Bt, N, D, dtype, stream, kBoth);
+}
+
+// The status words of the last adaln_bwd_noalloc on the current device sit at the head of
+// the fixed array, exactly where a caller workspace holds them.
+extern "C" int adaln_noalloc_read_status(cudaStream_t stream) {
+    void* scratch = nullptr;
+    if (int rc = noalloc_scratch(&scratch)) return rc;
+    return read_status_words(scratch, stream);
 }

@@ -121,7 +121,13 @@ size_t adaln_fwd_varlen_workspace_size(int64_t total_tokens, int32_t nseg, int64
                                        adaln_dtype dtype);
 
 /* Forward, packed mixed-length segments (x[total_tokens, D]); segment s uses modulation
- * row mod_idx[s] of shift/scale [nmod, D]. Same math as adaln_fwd. */
+ * row mod_idx[s] of shift/scale [nmod, D]. Same math as adaln_fwd. Section 2.A batches
+ * sequences of very different lengths into buckets (B sequences of length S each); the pages
+ * print no interface for feeding such a bucket to the operator. This call is the library's
+ * reading: the bucket's sequences packed back to back, delimited by the prefix sums
+ * cu_seqlens (segment s = rows [cu_seqlens[s], cu_seqlens[s+1])), each sequence with its
+ * own modulation row (the timestep / condition embedding of its sample), as section 2.B's
+ * per-sample modulation requires. The workspace receives the per-CTA status words. */
 int adaln_fwd_varlen(const void* x, const void* shift, const void* scale, void* y, float* mean,
                      float* rstd, const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
                      int64_t total_tokens, int64_t nmod, int64_t D, float eps, void* workspace,
@@ -131,8 +137,11 @@ int adaln_fwd_varlen(const void* x, const void* shift, const void* scale, void* 
 size_t adaln_bwd_varlen_workspace_size(int64_t total_tokens, int32_t nseg, int64_t nmod,
                                        int64_t D, adaln_dtype dtype);
 
-/* Backward, packed segments. dshift/dscale [nmod, D]: row m sums every token of every
- * segment with mod_idx == m, in a fixed order; rows no segment uses are written as 0. */
+/* Backward, packed segments (the layout of adaln_fwd_varlen, section 2.A buckets).
+ * dshift/dscale [nmod, D]: row m sums every token of every segment with mod_idx == m, in a
+ * fixed order; rows no segment uses are written as 0. Section 2.B, backward-pass bullet:
+ * the D-tile reduction runs down each (row tile, segment) piece, and the pieces of every
+ * modulation row are summed by the fixed-order second stage. */
 int adaln_bwd_varlen(const void* dy, const void* x, const float* mean, const float* rstd,
                      const void* scale, void* dx, float* dshift, float* dscale,
                      const int32_t* cu_seqlens, const int32_t* mod_idx, int32_t nseg,
@@ -198,10 +207,22 @@ int adaln_read_status(const void* workspace, cudaStream_t stream);
  *   - Every call on a device shares the one array, which keeps the last call's contents;
  *     nothing in it needs to start at zero. Calls that overlap on the GPU (different
  *     streams, or different host threads, without ordering between them) race on it and
- *     give wrong gradients: order them on one stream. */
+ *     give wrong gradients: order them on one stream.
+ *   - The device address is cached per device index for the life of the process; it does
+ *     not survive cudaDeviceReset (or any teardown of the device's primary context), after
+ *     which this call must not be used in that process.
+ *   - The kernels record device-side errors (a timed-out wait) in the array, where
+ *     adaln_read_status cannot see them: read them with adaln_noalloc_read_status. */
 int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean, const float* rstd,
                       const void* scale, void* dx, float* dshift, float* dscale, int64_t Bt,
                       int64_t N, int64_t D, adaln_dtype dtype, cudaStream_t stream);
+
+/* adaln_read_status for adaln_bwd_noalloc: synchronises `stream`, then returns the device-side
+ * status the last adaln_bwd_noalloc on the current device recorded in the library's fixed
+ * array (ADALN_OK or ADALN_ERR_TIMEOUT; ADALN_ERR_WORKSPACE before the first such call on the
+ * device, ADALN_ERR_CUDA if the copy fails). It copies a few bytes to the host and allocates
+ * nothing on the device. Like adaln_bwd_noalloc, this call has no counterpart in the paper. */
+int adaln_noalloc_read_status(cudaStream_t stream);
 
 /* Dual-constraint bucket size, AdaptiveLoad technical summary section 2.A:
  *     B = max(1, min(floor(M_mem / S), floor(M_comp / S^p)))

@@ -10,6 +10,9 @@ tolerances of the operator's parity bar:
 """
 from __future__ import annotations
 
+import os
+import threading
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 from typing import Optional
 
@@ -123,11 +126,14 @@ def gpu_bwd(d: DevWorkload, mean, rstd, packed: Optional[bool] = None):
 # ------------------------------------------------------------------------------------------
 # comparisons
 # ------------------------------------------------------------------------------------------
+# ulp of a bf16 value by its 8-bit exponent field e: 2^(e-134) for normal values (8
+# significant bits in the binade [2^(e-127), 2^(e-126))), and the smallest subnormal 2^-133
+# for zeros and subnormals.
+_BF16_ULP_BY_EXPONENT = np.array([2.0 ** -133] + [2.0 ** (e - 134) for e in range(1, 256)])
+
+
 def bf16_ulp(bits: np.ndarray) -> np.ndarray:
-    v = np.abs(synth.widen(bits, synth.BF16))
-    _, e = np.frexp(v)
-    ulp = np.ldexp(1.0, e - 8)
-    return np.maximum(ulp, 2.0 ** -133)
+    return _BF16_ULP_BY_EXPONENT[(np.asarray(bits, dtype=np.uint16) >> 7) & 0xFF]
 
 
 def check_io(gpu: np.ndarray, ref: np.ndarray, dtype: int, orc, what: str, extra=None):
@@ -183,3 +189,102 @@ def stat_shift_bound(ref_dx_terms):
     rstd, mean, xhat, mg, mgx = ref_dx_terms
     dm = np.spacing(np.abs(mean).astype(np.float32)).astype(np.float64)
     return (rstd * rstd * dm)[:, None] * (np.abs(mgx)[:, None] + np.abs(xhat) * np.abs(mg)[:, None]) * 1.01
+
+
+# ------------------------------------------------------------------------------------------
+# every row of a large workload against the oracle
+# ------------------------------------------------------------------------------------------
+CHUNK_ELEMENTS = 1 << 23  # elements of a row chunk (64 MB per float64 array)
+
+
+def workers() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def row_chunks(R: int, D: int):
+    n = max(1, CHUNK_ELEMENTS // D)
+    return [(a, min(R, a + n)) for a in range(0, R, n)]
+
+
+def mod_of_rows(w, r0: int, r1: int) -> np.ndarray:
+    seg = np.searchsorted(w.cu_seqlens, np.arange(r0, r1), side="right") - 1
+    return np.asarray(w.mod_idx)[seg]
+
+
+def dx_terms(w, mean, rstd, rows):
+    """Oracle-side quantities of rows [r0, r1) for stat_shift_bound."""
+    r0, r1 = rows
+    x = synth.widen(w.x[r0:r1], w.dtype)
+    dy = synth.widen(w.dy[r0:r1], w.dtype)
+    g = dy * (1 + synth.widen(w.scale, w.dtype)[mod_of_rows(w, r0, r1)])
+    xhat = (x - mean[:, None]) * rstd[:, None]
+    return rstd, mean, xhat, g.mean(axis=1), (g * xhat).mean(axis=1)
+
+
+def forward_all_rows(orc, w, y_h, mean_h, rstd_h, what=""):
+    """Every row of y, mean, rstd (host copies of the GPU outputs) against the oracle, a chunk
+    of rows at a time on a thread pool. Returns the oracle's statistics rounded to fp32 (as
+    float64 arrays), which the backward checks consume."""
+    m32 = np.empty(w.R)
+    r32 = np.empty(w.R)
+
+    def one(rows):
+        r0, r1 = rows
+        ry, rmean, rrstd = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod,
+                                   eps=EPS, rows=rows)
+        check_io(y_h[r0:r1], ry, w.dtype, orc, "%sy rows %d:%d" % (what, r0, r1))
+        check_stats(mean_h[r0:r1], rstd_h[r0:r1], rmean, rrstd, "%sstats rows %d:%d" % (what, r0, r1))
+        m32[r0:r1] = round_f32(rmean)
+        r32[r0:r1] = round_f32(rrstd)
+
+    with ThreadPoolExecutor(workers()) as ex:
+        list(ex.map(one, row_chunks(w.R, w.D)))
+    return m32, r32
+
+
+def backward_all_rows(orc, w, m32, r32, pipeline=None, isolated=None, what=""):
+    """Every row of dx and every row of dshift/dscale against the oracle's backward on the
+    oracle's fp32-rounded statistics (m32, r32). `isolated` = host (dx, dshift, dscale) of a
+    GPU backward that consumed those same statistics: strict tolerance. `pipeline` = host
+    (dx, dshift, dscale) of a GPU backward that consumed the GPU forward's own statistics:
+    dx gets the one-ulp mean-shift bound on top. dshift/dscale are checked row by row
+    (relative L2), and rows of the modulation table that no token uses must be exactly 0."""
+    lock = threading.Lock()
+    accs = []
+    local = threading.local()
+
+    def one(rows):
+        r0, r1 = rows
+        if not hasattr(local, "acc"):
+            local.acc = (np.zeros((w.nmod, w.D)), np.zeros((w.nmod, w.D)))
+            with lock:
+                accs.append(local.acc)
+        rdx, _, _ = orc.bwd(w.dy, w.x, m32[r0:r1], r32[r0:r1], w.scale, w.dtype, w.cu_seqlens,
+                            w.mod_idx, w.nmod, rows=rows, dshift=local.acc[0], dscale=local.acc[1])
+        if isolated is not None:
+            check_io(isolated[0][r0:r1], rdx, w.dtype, orc, "%sdx (isolated) rows %d:%d" % (what, r0, r1))
+        if pipeline is not None:
+            extra = stat_shift_bound(dx_terms(w, m32[r0:r1], r32[r0:r1], rows))
+            check_io(pipeline[0][r0:r1], rdx, w.dtype, orc, "%sdx (pipeline) rows %d:%d" % (what, r0, r1),
+                     extra=extra)
+
+    with ThreadPoolExecutor(workers()) as ex:
+        list(ex.map(one, row_chunks(w.R, w.D)))
+    ref_sh = np.zeros((w.nmod, w.D))
+    ref_sc = np.zeros((w.nmod, w.D))
+    for a_sh, a_sc in accs:
+        ref_sh += a_sh
+        ref_sc += a_sc
+    used = np.zeros(w.nmod, bool)
+    used[np.asarray(w.mod_idx)[np.diff(w.cu_seqlens) > 0]] = True
+    tol = grad_tol(w.dtype)
+    for label, got in (("isolated", isolated), ("pipeline", pipeline)):
+        if got is None:
+            continue
+        for name, g, ref in (("dshift", got[1], ref_sh), ("dscale", got[2], ref_sc)):
+            assert np.all(g[~used] == 0), "%s%s (%s): unused modulation rows not zero" % (what, name, label)
+            assert rel_l2(g, ref) <= tol, "%s%s (%s): whole table" % (what, name, label)
+            for m in np.nonzero(used)[0]:
+                e = rel_l2(g[m], ref[m])
+                assert e <= tol, "%s%s (%s) row %d: relative L2 %.3g" % (what, name, label, m, e)
+    return ref_sh, ref_sc

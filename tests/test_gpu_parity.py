@@ -1,8 +1,10 @@
 """CUDA path (through the C-ABI binding) against the CPU oracle on the same seeded bits.
 
-Small problems are compared element by element (several row tiles, ragged tails, odd
-segment tables, every row-width code path); the full-size workloads are compared on
-sampled rows and sampled modulation rows in the launch configuration the benchmark uses.
+Every case is compared element by element on every row: small problems (several row
+tiles, ragged tails, odd segment tables, every row-width code path and staging mode) and
+the full-size workloads in the launch configuration the benchmark uses, including each
+bucket of the packed workload as its own call. The oracle runs a chunk of rows at a time
+on a thread pool.
 """
 from __future__ import annotations
 
@@ -24,52 +26,30 @@ def cuda_ready():
     A.lib()  # loads the in-tree libadaln.so or raises
 
 
-def _oracle_full(orc, w, stats_rows=None):
-    y, mean, rstd = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod, eps=H.EPS)
-    return y, mean, rstd
-
-
-def _dx_terms(w, mean, rstd, rows):
-    """Oracle-side quantities for the statistics-shift bound of a pipeline comparison."""
-    x = synth.widen(w.x[rows[0]:rows[1]], w.dtype)
-    dy = synth.widen(w.dy[rows[0]:rows[1]], w.dtype)
-    m_of_row = np.repeat(w.mod_idx, np.diff(w.cu_seqlens))[rows[0]:rows[1]]
-    g = dy * (1 + synth.widen(w.scale, w.dtype)[m_of_row])
-    xhat = (x - mean[:, None]) * rstd[:, None]
-    return rstd, mean, xhat, g.mean(axis=1), (g * xhat).mean(axis=1)
-
-
 def _run_and_compare(orc, w):
+    """Forward, then two backwards: one on the oracle's statistics rounded to fp32 (isolated,
+    strict tolerance) and one on the GPU forward's own statistics (pipeline, plus the bound of
+    a one-ulp mean shift). Every row of y, mean, rstd and dx and every row of dshift/dscale
+    is compared with the oracle."""
+    t = H.torch()
     d = H.upload(w)
     y, mean, rstd, st = H.gpu_fwd(d)
     assert st == 0
-    ry, rmean, rrstd = _oracle_full(orc, w)
-    H.check_io(H.to_host(y, w.dtype), ry, w.dtype, orc, "y")
-    H.check_stats(H.to_host(mean, 0), H.to_host(rstd, 0), rmean, rrstd)
-
-    # Isolated backward: both sides consume the oracle's statistics rounded to fp32.
-    m32, r32 = H.round_f32(rmean), H.round_f32(rrstd)
-    t = H.torch()
+    dx2, dsh2, dsc2, st = H.gpu_bwd(d, mean, rstd)
+    assert st == 0
+    y_h, mean_h, rstd_h = H.to_host(y, w.dtype), H.to_host(mean, 0), H.to_host(rstd, 0)
+    pipeline = (H.to_host(dx2, w.dtype), H.to_host(dsh2, 0), H.to_host(dsc2, 0))
+    del y, dx2
+    m32, r32 = H.forward_all_rows(orc, w, y_h, mean_h, rstd_h)
+    del y_h
     dm = t.from_numpy(m32.astype(np.float32)).cuda()
     dr = t.from_numpy(r32.astype(np.float32)).cuda()
     dx, dsh, dsc, st = H.gpu_bwd(d, dm, dr)
     assert st == 0
-    rdx, rdsh, rdsc = orc.bwd(w.dy, w.x, m32, r32, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod)
-    H.check_io(H.to_host(dx, w.dtype), rdx, w.dtype, orc, "dx (isolated)")
-    assert H.rel_l2(H.to_host(dsh, 0), rdsh) <= H.grad_tol(w.dtype), "dshift (isolated)"
-    assert H.rel_l2(H.to_host(dsc, 0), rdsc) <= H.grad_tol(w.dtype), "dscale (isolated)"
-
-    # Pipeline backward: the GPU consumes its own forward statistics.
-    dx2, dsh2, dsc2, st = H.gpu_bwd(d, mean, rstd)
-    assert st == 0
-    extra = H.stat_shift_bound(_dx_terms(w, m32, r32, (0, w.R)))
-    H.check_io(H.to_host(dx2, w.dtype), rdx, w.dtype, orc, "dx (pipeline)", extra=extra)
-    assert H.rel_l2(H.to_host(dsh2, 0), rdsh) <= H.grad_tol(w.dtype), "dshift (pipeline)"
-    assert H.rel_l2(H.to_host(dsc2, 0), rdsc) <= H.grad_tol(w.dtype), "dscale (pipeline)"
-    # Rows of the modulation tables that no segment uses are exactly zero.
-    used = np.zeros(w.nmod, bool)
-    used[w.mod_idx[np.diff(w.cu_seqlens) > 0]] = True
-    assert np.all(H.to_host(dsh, 0)[~used] == 0) and np.all(H.to_host(dsc, 0)[~used] == 0)
+    isolated = (H.to_host(dx, w.dtype), H.to_host(dsh, 0), H.to_host(dsc, 0))
+    del d, dx
+    t.cuda.empty_cache()
+    H.backward_all_rows(orc, w, m32, r32, pipeline=pipeline, isolated=isolated)
 
 
 SMALL = {
@@ -126,6 +106,12 @@ SMALL = {
         list(np.random.default_rng(13).integers(0, 601, 700)), 601, dy_std=0.5),
     # One long segment spread over many row tiles, sharing its modulation row with
     # thousands of short ones.
+    # 90,008 bf16 rows of D=3072: more than 64 rows a resident CTA slot on GB300 (912 slots),
+    # so the forward stages them with its per-thread copy ring and maps them 3 x 128 threads,
+    # as on the packed benchmark workload; rows of two segments share modulation rows.
+    "packed-bf16-d3072-copy-ring": lambda: synth.make(
+        "c", 120, synth.BF16, 3072, [40000, 7, 50000, 1], [0, 1, 0, 1], 2,
+        x_mode=synth.ROWS_SCALED, dy_std=0.02),
     "packed-bf16-d256-long-and-many": lambda: synth.make(
         "c", 114, synth.BF16, 256, [5000] + list(np.random.default_rng(9).integers(1, 8, 2500)),
         [0] + list(np.random.default_rng(10).integers(0, 3, 2500)), 3,
@@ -138,86 +124,85 @@ def test_small_elementwise(orc, name):
     _run_and_compare(orc, SMALL[name]())
 
 
-def _oracle_rows(orc, w, r0, r1):
-    y, mean, rstd = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod,
-                            eps=H.EPS, rows=(r0, r1))
-    m32, r32 = H.round_f32(mean), H.round_f32(rstd)
-    dx, _, _ = orc.bwd(w.dy, w.x, m32, r32, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod,
-                       rows=(r0, r1))
-    return y, mean, rstd, dx, m32, r32
-
-
-def _sample_blocks(w, rng, per_segment=2, random_rows=48):
-    blocks = []
-    for s in range(w.nseg):
-        a, b = int(w.cu_seqlens[s]), int(w.cu_seqlens[s + 1])
-        if b > a:
-            blocks.append((a, min(b, a + per_segment)))
-            blocks.append((max(a, b - per_segment), b))
-    for r in rng.integers(0, w.R, random_rows):
-        blocks.append((int(r), int(r) + 1))
-    return sorted(set(blocks))
-
-
-def _full_size(orc, w, sample_mods):
-    t = H.torch()
-    d = H.upload(w)
-    y, mean, rstd, st = H.gpu_fwd(d)
-    assert st == 0
-    dx, dsh, dsc, st = H.gpu_bwd(d, mean, rstd)
-    assert st == 0
-    rng = np.random.default_rng(w.seed + 1000)
-    for r0, r1 in _sample_blocks(w, rng):
-        ry, rmean, rrstd, rdx, m32, r32 = _oracle_rows(orc, w, r0, r1)
-        H.check_io(H.to_host(y[r0:r1], w.dtype), ry, w.dtype, orc, "y rows %d:%d" % (r0, r1))
-        H.check_stats(H.to_host(mean[r0:r1], 0), H.to_host(rstd[r0:r1], 0), rmean, rrstd)
-        extra = H.stat_shift_bound(_dx_terms(w, m32, r32, (r0, r1)))
-        H.check_io(H.to_host(dx[r0:r1], w.dtype), rdx, w.dtype, orc, "dx rows %d:%d" % (r0, r1),
-                   extra=extra)
-    dsh_h, dsc_h = H.to_host(dsh, 0), H.to_host(dsc, 0)
-    for m in sample_mods:
-        ref_sh = np.zeros((w.nmod, w.D))
-        ref_sc = np.zeros((w.nmod, w.D))
-        for s in np.nonzero(w.mod_idx == m)[0]:
-            a, b = int(w.cu_seqlens[s]), int(w.cu_seqlens[s + 1])
-            for c0 in range(a, b, 8192):
-                c1 = min(b, c0 + 8192)
-                _, mu, rs = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod,
-                                    eps=H.EPS, rows=(c0, c1))
-                orc.bwd(w.dy, w.x, H.round_f32(mu), H.round_f32(rs), w.scale, w.dtype, w.cu_seqlens,
-                        w.mod_idx, w.nmod, rows=(c0, c1), dshift=ref_sh, dscale=ref_sc)
-        assert H.rel_l2(dsh_h[m], ref_sh[m]) <= H.grad_tol(w.dtype), "dshift[%d]" % m
-        assert H.rel_l2(dsc_h[m], ref_sc[m]) <= H.grad_tol(w.dtype), "dscale[%d]" % m
-    del d, y, dx
-    t.cuda.empty_cache()
+def _full_size(orc, w):
+    _run_and_compare(orc, w)
+    H.torch().cuda.empty_cache()
 
 
 def test_full_wan_1_3b(orc):
-    _full_size(orc, synth.config(1), [0])
+    _full_size(orc, synth.config(1))
 
 
 def test_full_wan_14b(orc):
-    _full_size(orc, synth.config(2), [0])
+    _full_size(orc, synth.config(2))
 
 
 def test_full_packed_buckets(orc):
     import adaln_layernorm_modulate_gb300 as A
     w = synth.config(3, bucket_batch=A.adaln_bucket_batch)
     assert w.meta["batches"] == [512, 128, 32, 2, 1, 1]
-    _full_size(orc, w, [0, 511, 512, 639, 640, 671, 673, 674, 675])
+    _full_size(orc, w)
 
 
-def test_full_bucket_s32760(orc):
-    # The packed workload's S=32760 bucket as its own call (one segment spanning every tile).
+@pytest.mark.parametrize("S", synth.BUCKET_S)
+def test_full_bucket_alone(orc, S):
+    # Each bucket of the packed workload as its own packed call: bucket_batch(S) segments of
+    # S tokens (S = 32760 and 75600: one segment spanning every row tile).
     import adaln_layernorm_modulate_gb300 as A
-    w = synth.bucket(32760, A.adaln_bucket_batch)
-    assert w.nseg == 1 and w.R == 32760
-    _full_size(orc, w, [0])
+    w = synth.bucket(S, A.adaln_bucket_batch)
+    assert w.nseg == A.adaln_bucket_batch(S, synth.BUCKET_M_MEM, synth.BUCKET_M_COMP, synth.BUCKET_P)
+    _full_size(orc, w)
 
 
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16], ids=["f32", "bf16"])
 def test_full_mmdit(orc, dtype):
-    _full_size(orc, synth.config(4, dtype=dtype), [0, 1, 2, 3])
+    _full_size(orc, synth.config(4, dtype=dtype))
+
+
+def test_shuffled_segment_order_gives_the_same_rows(orc):
+    """The packed workload with its 676 segments in a seeded random order (each segment
+    keeping its rows and its modulation row) gives, per segment, bitwise the y, mean, rstd
+    and dx of the ascending-order call: the row count and so the tiles' length and row
+    mapping are the same, and a row's arithmetic does not depend on which tile holds it.
+    dshift/dscale sum over other tile pieces, so they are compared with the oracle's."""
+    import adaln_layernorm_modulate_gb300 as A
+    t = H.torch()
+    w = synth.config(3, bucket_batch=A.adaln_bucket_batch)
+    perm = np.random.default_rng(2024).permutation(w.nseg)
+    lens = np.diff(w.cu_seqlens)
+    cu_p = np.zeros(w.nseg + 1, dtype=np.int64)
+    cu_p[1:] = np.cumsum(lens[perm])
+    # Row i of the shuffled batch is row src[i] of the ascending one.
+    src = np.concatenate([np.arange(w.cu_seqlens[s], w.cu_seqlens[s + 1]) for s in perm])
+    d = H.upload(w)
+    y, mean, rstd, st = H.gpu_fwd(d)
+    assert st == 0
+    dx, dsh, dsc, st = H.gpu_bwd(d, mean, rstd)
+    assert st == 0
+    idx = t.from_numpy(src).cuda()
+    ws = synth.Workload("shuffled", w.seed, w.dtype, w.D, cu_p, w.mod_idx[perm].copy(), w.nmod,
+                        x=None, dy=None, shift=w.shift, scale=w.scale)
+    dp = H.DevWorkload(ws, d.x[idx], d.dy[idx], d.shift, d.scale,
+                       t.from_numpy(cu_p.astype(np.int32)).cuda(),
+                       t.from_numpy(ws.mod_idx.astype(np.int32)).cuda())
+    y2, mean2, rstd2, st = H.gpu_fwd(dp)
+    assert st == 0
+    assert t.equal(y2, y[idx]) and t.equal(mean2, mean[idx]) and t.equal(rstd2, rstd[idx])
+    del y, y2, d.x
+    t.cuda.empty_cache()
+    dx2, dsh2, dsc2, st = H.gpu_bwd(dp, mean2, rstd2)
+    assert st == 0
+    assert t.equal(dx2, dx[idx])
+    del dx, dx2, dp, d
+    t.cuda.empty_cache()
+    # The gradients of every modulation row against the oracle on the ascending rows (the
+    # same token sets), with the GPU forward's statistics in both orders being bitwise equal.
+    m32, r32 = H.round_f32(H.to_host(mean, 0).astype(np.float64)), H.round_f32(H.to_host(rstd, 0).astype(np.float64))
+    ref_sh, ref_sc = H.backward_all_rows(orc, w, m32, r32)
+    for got, ref in ((dsh2, ref_sh), (dsc2, ref_sc)):
+        g = H.to_host(got, 0)
+        for m in range(w.nmod):
+            assert H.rel_l2(g[m], ref[m]) <= H.grad_tol(w.dtype), m
 
 
 def test_backward_is_bitwise_deterministic():
@@ -378,16 +363,6 @@ def test_outputs_stay_inside_their_buffers():
         assert intact(buf, n)
 
 
-# Too large for the element-by-element oracle cases, compared GPU against GPU: 90,008 bf16
-# rows of D=3072 are more than 64 rows a resident CTA slot on GB300 (912 slots), so the
-# forward stages them with its per-thread copy ring and maps them 3 x 128 threads.
-RECOMPUTE_ONLY = {
-    "packed-bf16-d3072-copy-ring": lambda: synth.make(
-        "c", 120, synth.BF16, 3072, [40000, 7, 50000, 1], [0, 1, 0, 1], 2,
-        x_mode=synth.ROWS_SCALED, dy_std=0.02),
-}
-
-
 @pytest.mark.parametrize("name", ["dense-bf16-2x300x1536", "packed-bf16-d3072-ragged",
                                   "packed-f32-d3072-adversarial", "dense-bf16-d16384",
                                   "packed-bf16-d8-long-tiles", "packed-bf16-d3072-copy-ring"])
@@ -396,7 +371,7 @@ def test_recomputed_statistics_are_bitwise_the_saved_ones(name):
     the backward that reads the forward's saved statistics."""
     import adaln_layernorm_modulate_gb300 as A
     t = H.torch()
-    w = (SMALL.get(name) or RECOMPUTE_ONLY[name])()
+    w = SMALL[name]()
     d = H.upload(w)
     y, mean, rstd, _ = H.gpu_fwd(d)
     dx, dsh, dsc, _ = H.gpu_bwd(d, mean, rstd)
