@@ -23,6 +23,7 @@ namespace adaln {
 
 template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
 __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) bwd_kernel(const BwdArgs a) {
+    pdl_begin();
     using IO = Io<T>;
     constexpr int VE = IO::VE;
     constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector
@@ -129,19 +130,24 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) bwd_kernel(const B
 #pragma unroll
         for (int p = 0; p < PV; ++p) acc_dy[k][p] = acc_dyx[k][p] = kPairZero;
 
-    // Piece (tile b, segment cur_s) done: one fp32 partial row pair in slot b + cur_s.
+    // Piece (tile b, segment cur_s) done: each thread writes its vectors' column sums into
+    // slot b + cur_s, in the layout the launch chose (see BwdArgs).
+    const int64_t S = G + a.seg.nseg;
     auto flush = [&]() {
-        float* P = a.partials + (b + cur_s) * 2 * D;
+        const int64_t slot = b + cur_s;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             if (ok[k]) {
-                float* pk = P + colb[k] / sizeof(T);  // element offset of my vector k
+                const int64_t v = colb[k] / 16;  // my vector k
+                float* p0 = a.vec_major ? a.partials + ((v * 2 + 0) * S + slot) * VE
+                                        : a.partials + slot * 2 * D + v * VE;
+                float* p1 = a.vec_major ? a.partials + ((v * 2 + 1) * S + slot) * VE : p0 + D;
 #pragma unroll
                 for (int p = 0; p < PV; p += 2) {
                     const float2 a0 = p_get(acc_dy[k][p]), a1 = p_get(acc_dy[k][p + 1]);
                     const float2 b0 = p_get(acc_dyx[k][p]), b1 = p_get(acc_dyx[k][p + 1]);
-                    *reinterpret_cast<float4*>(pk + 2 * p) = make_float4(a0.x, a0.y, a1.x, a1.y);
-                    *reinterpret_cast<float4*>(pk + D + 2 * p) = make_float4(b0.x, b0.y, b1.x, b1.y);
+                    *reinterpret_cast<float4*>(p0 + 2 * p) = make_float4(a0.x, a0.y, a1.x, a1.y);
+                    *reinterpret_cast<float4*>(p1 + 2 * p) = make_float4(b0.x, b0.y, b1.x, b1.y);
                 }
             }
 #pragma unroll
@@ -355,14 +361,228 @@ constexpr int kStage2Per = 4;
 constexpr int kStage2Chunk = kStage2Threads * kStage2Per;
 constexpr int kStage2Unroll = 4;
 
+// Compacts entries [base, base + kStage2Chunk) of the segment table whose modulation row is m
+// into hit_slot (partial slot of the hit's first piece) and hit_first (flat index of that
+// piece among the hits'), in table order: H hits, NP pieces, hit_first[H] = NP. Every thread
+// of a kStage2Threads-thread CTA calls it; it ends with a barrier.
+__device__ __forceinline__ void compact_hits(const Segments& sg, int64_t m, int64_t base, int64_t R, int64_t G,
+                                             uint32_t* hit_slot, int32_t* hit_first,
+                                             int32_t (*warp_tot)[kStage2Threads / 32], int& H, int& NP) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // This thread's entries: segments s0 .. s0 + kStage2Per - 1 of the chunk.
+    const int64_t s0 = base + (int64_t)tid * kStage2Per;
+    int32_t np[kStage2Per];
+    uint32_t sl[kStage2Per];
+    int hc = 0, pc = 0;
+#pragma unroll
+    for (int i = 0; i < kStage2Per; ++i) {
+        const int64_t s = s0 + i;
+        np[i] = 0;
+        sl[i] = 0;
+        if (s < sg.nseg && (int64_t)__ldg(sg.mod + s) == m) {
+            // Clamp into [0, R] so a malformed table cannot index past the slots.
+            const int64_t lo = max((int64_t)0, min(seg_start<true>(sg, s), R));
+            const int64_t hi = max((int64_t)0, min(seg_start<true>(sg, s + 1), R));
+            if (hi > lo) {
+                const int64_t blo = tile_of_row(lo, R, G), bhi = tile_of_row(hi - 1, R, G);
+                np[i] = (int32_t)(bhi - blo + 1);
+                sl[i] = (uint32_t)(blo + s);
+                ++hc;
+                pc += np[i];
+            }
+        }
+    }
+    // Block-wide exclusive scan of (hits, pieces) in thread order = table order.
+    int ih = hc, ip = pc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int th = __shfl_up_sync(0xFFFFFFFFu, ih, o);
+        const int tp = __shfl_up_sync(0xFFFFFFFFu, ip, o);
+        if (lane >= o) {
+            ih += th;
+            ip += tp;
+        }
+    }
+    if (lane == 31) {
+        warp_tot[0][warp] = ih;
+        warp_tot[1][warp] = ip;
+    }
+    __syncthreads();
+    int oh = ih - hc, op = ip - pc;
+    H = 0;
+    NP = 0;
+#pragma unroll
+    for (int w = 0; w < kStage2Threads / 32; ++w) {
+        const int th = warp_tot[0][w], tp = warp_tot[1][w];
+        if (w < warp) {
+            oh += th;
+            op += tp;
+        }
+        H += th;
+        NP += tp;
+    }
+#pragma unroll
+    for (int i = 0; i < kStage2Per; ++i) {
+        if (np[i] > 0) {
+            hit_slot[oh] = sl[i];
+            hit_first[oh] = op;
+            ++oh;
+            op += np[i];
+        }
+    }
+    if (tid == 0) hit_first[H] = NP;
+    __syncthreads();
+}
+
+// The hit holding piece q of a compacted list: the last h with hit_first[h] <= q; returns
+// the piece's partial slot.
+__device__ __forceinline__ int64_t hit_slot_of(int64_t q, int H, const uint32_t* hit_slot,
+                                               const int32_t* hit_first) {
+    int lo = 0, hi = H - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)hit_first[mid] <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    return (int64_t)hit_slot[lo] + (q - (int64_t)hit_first[lo]);
+}
+
+// Stage 2 over vector-major partials (modulation rows with many pieces). CTA (blockIdx.x, m)
+// covers nvb = kStage2Threads / splits consecutive 16-byte vectors of columns; `splits`
+// consecutive threads share one vector, piece j going to thread j mod splits, which adds its
+// pieces in list order. A vector's pieces sit side by side, so the threads of a vector read
+// consecutive 32-byte (bf16) or 16-byte (fp32) chunks. The threads' sums are then combined
+// by a fixed tree: shuffles within a warp, then the vector's warps in warp order.
+template <int VE, bool VARLEN>
+__global__ void __launch_bounds__(kStage2Threads) stage2v_kernel(const Stage2Args a) {
+    pdl_begin();
+    constexpr int Q = VE / 4;  // float4 per vector
+    constexpr int NW = kStage2Threads / 32;
+    __shared__ float red[NW][2 * VE];
+    __shared__ uint32_t hit_slot[kStage2Chunk];
+    __shared__ int32_t hit_first[kStage2Chunk + 1];
+    __shared__ int32_t warp_tot[2][NW];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int splits = a.splits, nvb = kStage2Threads / splits;
+    const int k = tid % splits, vj = tid / splits;
+    const int64_t V = a.D / VE, S = a.S;
+    const int64_t v = (int64_t)blockIdx.x * nvb + vj;
+    const bool vok = v < V;
+    const int64_t R = a.seg.R, G = a.G;
+    const float4* P0 = reinterpret_cast<const float4*>(a.partials) + (v * 2 + 0) * S * Q;
+    const float4* P1 = reinterpret_cast<const float4*>(a.partials) + (v * 2 + 1) * S * Q;
+
+    for (int64_t m = blockIdx.y; m < a.seg.nmod; m += gridDim.y) {
+        float acc[2 * VE];
+#pragma unroll
+        for (int e = 0; e < 2 * VE; ++e) acc[e] = 0.0f;
+        int64_t J = 0;  // pieces of row m before the current list
+
+        auto sum_pieces = [&](int64_t n, auto slot_of) {
+            if (vok) {
+                int64_t q0 = ((int64_t)k - J) % splits;
+                if (q0 < 0) q0 += splits;
+                for (; q0 < n; q0 += (int64_t)kStage2Unroll * splits) {
+                    float4 u[kStage2Unroll][Q], w[kStage2Unroll][Q];
+#pragma unroll
+                    for (int i = 0; i < kStage2Unroll; ++i) {
+                        const int64_t q = q0 + (int64_t)i * splits;
+                        if (q < n) {
+                            const int64_t slot = slot_of(q);
+#pragma unroll
+                            for (int j = 0; j < Q; ++j) {
+                                u[i][j] = __ldg(P0 + slot * Q + j);
+                                w[i][j] = __ldg(P1 + slot * Q + j);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kStage2Unroll; ++i) {
+                        if (q0 + (int64_t)i * splits < n) {
+#pragma unroll
+                            for (int j = 0; j < Q; ++j) {
+                                acc[4 * j + 0] += u[i][j].x; acc[4 * j + 1] += u[i][j].y;
+                                acc[4 * j + 2] += u[i][j].z; acc[4 * j + 3] += u[i][j].w;
+                                acc[VE + 4 * j + 0] += w[i][j].x; acc[VE + 4 * j + 1] += w[i][j].y;
+                                acc[VE + 4 * j + 2] += w[i][j].z; acc[VE + 4 * j + 3] += w[i][j].w;
+                            }
+                        }
+                    }
+                }
+            }
+            J += n;
+        };
+
+        if constexpr (!VARLEN) {
+            const int64_t lo = min(m * a.seg.N, R), hi = min((m + 1) * a.seg.N, R);
+            if (hi > lo) {
+                const int64_t blo = tile_of_row(lo, R, G), bhi = tile_of_row(hi - 1, R, G);
+                sum_pieces(bhi - blo + 1, [&](int64_t q) { return blo + q + m; });
+            }
+        } else {
+            for (int64_t base = 0; base < a.seg.nseg; base += kStage2Chunk) {
+                int H = 0, NP = 0;
+                compact_hits(a.seg, m, base, R, G, hit_slot, hit_first, warp_tot, H, NP);
+                if (H > 0) sum_pieces(NP, [&](int64_t q) { return hit_slot_of(q, H, hit_slot, hit_first); });
+                __syncthreads();  // the next chunk reuses the hit lists and warp totals
+            }
+        }
+
+        if (splits <= 32) {
+            // The vector's threads are `splits` consecutive lanes of one warp.
+            for (int o = 1; o < splits; o <<= 1) {
+#pragma unroll
+                for (int e = 0; e < 2 * VE; ++e) acc[e] += __shfl_xor_sync(0xFFFFFFFFu, acc[e], o);
+            }
+            if (k == 0 && vok) {
+                float4* o0 = reinterpret_cast<float4*>(a.dshift + m * a.D + v * VE);
+                float4* o1 = reinterpret_cast<float4*>(a.dscale + m * a.D + v * VE);
+#pragma unroll
+                for (int j = 0; j < Q; ++j) {
+                    o0[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                    o1[j] = make_float4(acc[VE + 4 * j], acc[VE + 4 * j + 1], acc[VE + 4 * j + 2],
+                                        acc[VE + 4 * j + 3]);
+                }
+            }
+        } else {
+            // The vector's threads fill splits / 32 whole warps: a butterfly in each warp,
+            // then the warps' sums in warp order.
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+                for (int e = 0; e < 2 * VE; ++e) acc[e] += __shfl_xor_sync(0xFFFFFFFFu, acc[e], o);
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int e = 0; e < 2 * VE; ++e) red[warp][e] = acc[e];
+            }
+            __syncthreads();
+            const int wpv = splits / 32;
+            if (tid < nvb * 2 * VE) {
+                const int vv = tid / (2 * VE), e = tid % (2 * VE);
+                const int64_t vg = (int64_t)blockIdx.x * nvb + vv;
+                if (vg < V) {
+                    float t = red[vv * wpv][e];
+                    for (int w2 = 1; w2 < wpv; ++w2) t += red[vv * wpv + w2][e];
+                    float* out = e < VE ? a.dshift : a.dscale;
+                    out[m * a.D + vg * VE + (e % VE)] = t;
+                }
+            }
+        }
+        __syncthreads();  // the next row reuses the shared lists and sums
+    }
+}
+
 template <bool VARLEN>
 __global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2Args a) {
+    pdl_begin();
     __shared__ float4 red[2][kStage2Threads];
     __shared__ uint32_t hit_slot[kStage2Chunk];       // partial slot of the hit's first piece
     __shared__ int32_t hit_first[kStage2Chunk + 1];   // flat index of the hit's first piece
     __shared__ int32_t warp_tot[2][kStage2Threads / 32];
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int cw = a.cw, splits = kStage2Threads / cw;
     const int ci = tid % cw, k = tid / cw;
     const int64_t D4 = a.D / 4;
@@ -411,79 +631,9 @@ __global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2A
             }
         } else {
             for (int64_t base = 0; base < a.seg.nseg; base += kStage2Chunk) {
-                // This thread's entries: segments s0 .. s0 + kStage2Per - 1 of the chunk.
-                const int64_t s0 = base + (int64_t)tid * kStage2Per;
-                int32_t np[kStage2Per];
-                uint32_t sl[kStage2Per];
-                int hc = 0, pc = 0;
-#pragma unroll
-                for (int i = 0; i < kStage2Per; ++i) {
-                    const int64_t s = s0 + i;
-                    np[i] = 0;
-                    sl[i] = 0;
-                    if (s < a.seg.nseg && (int64_t)__ldg(a.seg.mod + s) == m) {
-                        // Clamp into [0, R] so a malformed table cannot index past the slots.
-                        const int64_t lo = max((int64_t)0, min(seg_start<true>(a.seg, s), R));
-                        const int64_t hi = max((int64_t)0, min(seg_start<true>(a.seg, s + 1), R));
-                        if (hi > lo) {
-                            const int64_t blo = tile_of_row(lo, R, G), bhi = tile_of_row(hi - 1, R, G);
-                            np[i] = (int32_t)(bhi - blo + 1);
-                            sl[i] = (uint32_t)(blo + s);
-                            ++hc;
-                            pc += np[i];
-                        }
-                    }
-                }
-                // Block-wide exclusive scan of (hits, pieces) in thread order = table order.
-                int ih = hc, ip = pc;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int th = __shfl_up_sync(0xFFFFFFFFu, ih, o);
-                    const int tp = __shfl_up_sync(0xFFFFFFFFu, ip, o);
-                    if (lane >= o) {
-                        ih += th;
-                        ip += tp;
-                    }
-                }
-                if (lane == 31) {
-                    warp_tot[0][warp] = ih;
-                    warp_tot[1][warp] = ip;
-                }
-                __syncthreads();
-                int oh = ih - hc, op = ip - pc, H = 0, NP = 0;
-#pragma unroll
-                for (int w = 0; w < kStage2Threads / 32; ++w) {
-                    const int th = warp_tot[0][w], tp = warp_tot[1][w];
-                    if (w < warp) {
-                        oh += th;
-                        op += tp;
-                    }
-                    H += th;
-                    NP += tp;
-                }
-#pragma unroll
-                for (int i = 0; i < kStage2Per; ++i) {
-                    if (np[i] > 0) {
-                        hit_slot[oh] = sl[i];
-                        hit_first[oh] = op;
-                        ++oh;
-                        op += np[i];
-                    }
-                }
-                if (tid == 0) hit_first[H] = NP;
-                __syncthreads();
-                if (H > 0) {
-                    sum_pieces(NP, [&](int64_t q) {
-                        // The hit holding piece q: the last h with hit_first[h] <= q.
-                        int lo = 0, hi = H - 1;
-                        while (lo < hi) {
-                            const int mid = (lo + hi + 1) >> 1;
-                            if ((int64_t)hit_first[mid] <= q) lo = mid;
-                            else hi = mid - 1;
-                        }
-                        return (int64_t)hit_slot[lo] + (q - (int64_t)hit_first[lo]);
-                    });
-                }
+                int H = 0, NP = 0;
+                compact_hits(a.seg, m, base, R, G, hit_slot, hit_first, warp_tot, H, NP);
+                if (H > 0) sum_pieces(NP, [&](int64_t q) { return hit_slot_of(q, H, hit_slot, hit_first); });
                 __syncthreads();  // the next chunk reuses the hit lists and warp totals
             }
         }
@@ -557,17 +707,37 @@ cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool
     if (!fn) return cudaErrorInvalidValue;
     BwdArgs a = args;
     void* params[] = {&a};
-    return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream);
+    return launch_dependent(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream);
 }
 
-cudaError_t launch_stage2(const Stage2Args& args, bool varlen, cudaStream_t stream) {
-    const int64_t D4 = args.D / 4;
-    const int64_t gy = args.seg.nmod < 65535 ? args.seg.nmod : 65535;
-    const dim3 grid((unsigned)((D4 + args.cw - 1) / args.cw), (unsigned)gy);
+cudaError_t launch_stage2(const Stage2Args& args, int dtype, bool varlen, int sms, cudaStream_t stream) {
+    dim3 grid;
+    const void* fn;
+    const unsigned gy = (unsigned)(args.seg.nmod < 65535 ? args.seg.nmod : 65535);
+    if (args.vec_major) {
+        const int VE = dtype == 1 ? 8 : 4;
+        const int64_t nvb = kStage2Threads / args.splits;
+        grid = dim3((unsigned)((args.D / VE + nvb - 1) / nvb), gy);
+        fn = dtype == 1 ? (varlen ? reinterpret_cast<const void*>(&stage2v_kernel<8, true>)
+                                  : reinterpret_cast<const void*>(&stage2v_kernel<8, false>))
+                        : (varlen ? reinterpret_cast<const void*>(&stage2v_kernel<4, true>)
+                                  : reinterpret_cast<const void*>(&stage2v_kernel<4, false>));
+    } else {
+        grid = dim3((unsigned)((args.D / 4 + args.cw - 1) / args.cw), gy);
+        fn = varlen ? reinterpret_cast<const void*>(&stage2_kernel<true>)
+                    : reinterpret_cast<const void*>(&stage2_kernel<false>);
+    }
     Stage2Args a = args;
     void* params[] = {&a};
-    const void* fn = varlen ? reinterpret_cast<const void*>(&stage2_kernel<true>)
-                            : reinterpret_cast<const void*>(&stage2_kernel<false>);
+    // A stage 2 of one wave starts as a dependent of the backward (its CTAs take the SMs the
+    // backward's CTAs leave, then wait for it to complete): bf16 D=1536 on 32,760 rows with
+    // vector-major partials, 97.6 -> 94.8 us a step. One of several waves measured slower that
+    // way (the packed D=3072 workload: 2506 -> 2544 us a step), so it waits in the stream.
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kStage2Threads, 0);
+    if (e != cudaSuccess) return e;
+    if ((int64_t)grid.x * grid.y <= (int64_t)per_sm * sms)
+        return launch_dependent(fn, grid, dim3(kStage2Threads), params, 0, stream);
     return cudaLaunchKernel(fn, grid, dim3(kStage2Threads), params, 0, stream);
 }
 

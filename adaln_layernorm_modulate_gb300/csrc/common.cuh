@@ -80,7 +80,15 @@ struct BwdArgs {
     const float* rstd;
     const void* scale;
     void* dx;
-    float* partials;     // [G + nseg][2][D]: slot b + s holds CTA b's sums over segment s
+    // Per-piece fp32 column sums of dy (q = 0) and dy * xhat (q = 1) over piece slot b + s
+    // (CTA b's rows of segment s), S = G + nseg slots, in one of two layouts:
+    //   row-major     partials[(slot * 2 + q) * D + column]: a piece is one contiguous row,
+    //                 for modulation rows with few pieces each (a row is read whole);
+    //   vector-major  partials[((v * 2 + q) * S + slot) * VE + e], column = v * VE + e: one
+    //                 16-byte vector's pieces sit side by side, for rows with many pieces
+    //                 (their pieces are read down the slots).
+    float* partials;
+    int vec_major;
     int64_t D;
     Segments seg;
     uint32_t* status;
@@ -89,12 +97,15 @@ struct BwdArgs {
 };
 
 struct Stage2Args {
-    const float* partials;
+    const float* partials;  // the backward's, in the layout vec_major names
     float* dshift;
     float* dscale;
     int64_t D;
     int64_t G;           // row tiles of the backward launch
-    int cw;              // float4 columns per CTA (power of two, <= kStage2Threads)
+    int64_t S;           // partial slots: G + nseg
+    int vec_major;
+    int cw;              // row-major: float4 columns per CTA (power of two, <= kStage2Threads)
+    int splits;          // vector-major: threads summing one vector (power of two, <= kStage2Threads)
     Segments seg;
 };
 
@@ -304,6 +315,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
             }
         }
     }
+}
+
+// ---------------------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel is launched so that it may be scheduled before
+// the kernel ahead of it in the stream has finished: its CTAs take SMs as that kernel's CTAs
+// retire. Each kernel first lets its own dependents be scheduled, then waits, before any
+// global memory access, until the kernel ahead has completed and its writes are visible.
+// Without such a kernel ahead (a copy, an event, a kernel launched without the attribute)
+// the wait returns at once. This hides a launch's scheduling and set-up behind the end of
+// the previous kernel; nothing is read or written early.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+inline cudaError_t launch_dependent(const void* fn, dim3 grid, dim3 block, void** params, size_t smem,
+                                    cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, params);
 }
 
 // Lets `fn` use, with its static shared memory, up to the device's opt-in shared memory per

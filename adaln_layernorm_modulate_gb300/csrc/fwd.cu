@@ -33,6 +33,7 @@ namespace adaln {
 
 template <typename T, int NV, bool VARLEN, int RING, bool FULL>
 __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const FwdArgs a) {
+    pdl_begin();
     constexpr bool BULK = RING == kRingBulk, COPY = RING == kRingCopy;
     using IO = Io<T>;
     constexpr int VE = IO::VE;
@@ -365,7 +366,7 @@ cudaError_t launch_fwd(const FwdArgs& args, int dtype, int nv, bool varlen, int 
     if (!fn) return cudaErrorInvalidValue;
     FwdArgs a = args;
     void* params[] = {&a};
-    return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream);
+    return launch_dependent(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream);
 }
 
 // Row statistics alone, for a backward whose forward kept no statistics: the forward's row
@@ -377,6 +378,7 @@ template <typename T, int NV>
 __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) stats_kernel(const void* x, float* mean,
                                                                          float* rstd, int64_t R, int64_t D,
                                                                          float eps) {
+    pdl_begin();
     using IO = Io<T>;
     constexpr int VE = IO::VE;
     constexpr int PV = VE / 2;
@@ -491,7 +493,7 @@ cudaError_t launch_stats(const void* x, float* mean, float* rstd, int64_t R, int
     const void* fn = dtype == 0 ? pick_stats<float>(nv) : dtype == 1 ? pick_stats<__nv_bfloat16>(nv) : nullptr;
     if (!fn || G < 1) return cudaErrorInvalidValue;
     void* params[] = {&x, &mean, &rstd, &R, &D, &eps};
-    return cudaLaunchKernel(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, 0, stream);
+    return launch_dependent(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, 0, stream);
 }
 
 }  // namespace adaln

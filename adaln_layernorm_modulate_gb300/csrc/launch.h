@@ -24,6 +24,7 @@ cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool fu
                               size_t smem, int* out);
 cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
                        int64_t G, int tpb, size_t smem, cudaStream_t stream);
-cudaError_t launch_stage2(const Stage2Args& args, bool varlen, cudaStream_t stream);
+// Stage 2 of a backward on a device of `sms` multiprocessors.
+cudaError_t launch_stage2(const Stage2Args& args, int dtype, bool varlen, int sms, cudaStream_t stream);
 
 }  // namespace adaln

@@ -106,6 +106,42 @@ class Oracle:
             raise ValueError("oracle_adaln_bwd rejected its arguments")
         return dx, dshift, dscale
 
+    def fwd_bwd_blocks(self, x, dy, shift, scale, dtype, cu_seqlens, mod_idx, nmod, rows, threads,
+                       eps=1e-6, block_rows=1024):
+        """Forward, then backward on the forward's statistics rounded to fp32 (as a caller that
+        saves them in fp32 would), over rows [r0, r1), in blocks of `block_rows` rows spread over
+        `threads` host threads (the library calls release the interpreter lock). Per-row
+        outputs are discarded; returns the (dshift, dscale) sums. Used to time the oracle on
+        all cores; each block is the plain per-row code above."""
+        from concurrent.futures import ThreadPoolExecutor
+        import threading
+
+        r0, r1 = rows
+        D = x.shape[-1]
+        local = threading.local()
+        accs = []
+        lock = threading.Lock()
+
+        def one(b0):
+            b1 = min(r1, b0 + block_rows)
+            if not hasattr(local, "acc"):
+                local.acc = (np.zeros((nmod, D)), np.zeros((nmod, D)))
+                with lock:
+                    accs.append(local.acc)
+            _, mean, rstd = self.fwd(x, shift, scale, dtype, cu_seqlens, mod_idx, nmod, eps=eps,
+                                     rows=(b0, b1))
+            self.bwd(dy, x, mean.astype(np.float32), rstd.astype(np.float32), scale, dtype, cu_seqlens,
+                     mod_idx, nmod, rows=(b0, b1), dshift=local.acc[0], dscale=local.acc[1])
+
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(r0, r1, block_rows)))
+        dsh = np.zeros((nmod, D))
+        dsc = np.zeros((nmod, D))
+        for a, b in accs:
+            dsh += a
+            dsc += b
+        return dsh, dsc
+
     def round_bf16(self, v) -> np.ndarray:
         v = _c(np.asarray(v), np.float64)
         out = np.empty(v.shape, np.uint16)

@@ -34,3 +34,27 @@ def test_e2e_chunks_refuse_shared_or_permuted_tables():
     # Identity tables split at the first segment boundary at or after each token quantile.
     w = synth.make("c", 1, synth.BF16, 64, [5, 6, 7, 8], None, None, generate=False)
     assert bench.e2e_chunks(w, 2) == [(0, 3), (3, 4)]
+
+
+def test_literal_bytes_count_each_tensor_once():
+    # read x, dy, shift, scale; write y, dx, mean, rstd, dshift, dscale
+    R, D, e, nmod = 1000, 3072, 2, 3
+    want = (R * D * e) * 4 + 4 * R * 2 + nmod * D * e * 2 + nmod * D * 4 * 2
+    assert bench.literal_bytes(R, D, e, nmod) == want
+    # Against the per-call sums: x is read by both calls and the statistics are written by
+    # the forward and read by the backward, so without modulation rows the calls' row
+    # traffic is 5/4 of the literal count's.
+    nb = bench.algorithmic_bytes(R, D, e, 0)
+    assert nb["step"] - 16 * R == 5 * (bench.literal_bytes(R, D, e, 0) - 8 * R) // 4
+
+
+def test_oracle_blocks_on_threads_sum_like_one_pass(orc):
+    import numpy as np
+    w = synth.make("blk", 9, synth.F32, 64, [300, 5, 1200], [1, 0, 1], 2, dy_std=0.5)
+    _, mean, rstd = orc.fwd(w.x, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod)
+    _, dsh, dsc = orc.bwd(w.dy, w.x, mean.astype(np.float32), rstd.astype(np.float32), w.scale, w.dtype,
+                          w.cu_seqlens, w.mod_idx, w.nmod)
+    bsh, bsc = orc.fwd_bwd_blocks(w.x, w.dy, w.shift, w.scale, w.dtype, w.cu_seqlens, w.mod_idx, w.nmod,
+                                  (0, w.R), 4, block_rows=100)
+    np.testing.assert_allclose(bsh, dsh, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(bsc, dsc, rtol=1e-12, atol=1e-12)

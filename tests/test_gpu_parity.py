@@ -394,3 +394,25 @@ def test_recomputed_statistics_are_bitwise_the_saved_ones(name):
     assert t.equal(dsh, dsh2) and t.equal(dsc, dsc2)
     del d, y, dx, dx2
     t.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xFF, 0x5A])
+def test_workspace_contents_do_not_matter(fill):
+    """The backward's workspace needs no initialisation: zeroed, all-ones and patterned
+    workspaces, reused call after call, give bitwise the results of a fresh one."""
+    import adaln_layernorm_modulate_gb300 as A
+    t = H.torch()
+    w = synth.make("ws", 130, synth.BF16, 3072, [40, 3000, 1, 0, 9000, 513], [5, 0, 2, 2, 1, 0], 7,
+                   x_mode=synth.ROWS_SCALED, dy_std=0.02)
+    d = H.upload(w)
+    _, mean, rstd, _ = H.gpu_fwd(d)
+    ref = H.gpu_bwd(d, mean, rstd)[:3]
+    nb = A.adaln_bwd_varlen_workspace_size(w.R, w.nseg, w.nmod, w.D, w.dtype)
+    ws = t.full((nb,), fill, dtype=t.uint8, device="cuda")
+    for _ in range(3):
+        dx = t.empty_like(ref[0])
+        dsh, dsc = t.empty_like(ref[1]), t.empty_like(ref[2])
+        A.adaln_bwd_varlen(d.dy, d.x, mean, rstd, d.scale, dx, dsh, dsc, d.cu, d.mod, w.nseg, w.R,
+                           w.nmod, w.D, ws, nb, w.dtype)
+        assert A.adaln_read_status(ws) == 0
+        assert t.equal(dx, ref[0]) and t.equal(dsh, ref[1]) and t.equal(dsc, ref[2])

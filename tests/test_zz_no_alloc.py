@@ -82,3 +82,14 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = _noalloc(d, mean, rstd, dx, dsh, dsc)
     assert A.STATUS[rc] == "ADALN_ERR_WORKSPACE"
     t.cuda.synchronize()
+
+
+def test_noalloc_status_is_readable():
+    """adaln_noalloc_read_status reads the status words a backward leaves at the head of the
+    fixed array: after a call they read as OK (the array is zero when the library loads, so
+    before the first call on a device there is no status to read)."""
+    import adaln_layernorm_modulate_gb300 as A
+    before = A.STATUS[A.adaln_noalloc_read_status()]
+    assert before in ("ADALN_ERR_WORKSPACE", "ADALN_OK"), before  # OK if a test above ran first
+    _compare(synth.dense("na4", 704, synth.BF16, 1, 3000, 1536, x_mode=synth.ROWS_SCALED, dy_std=0.02))
+    assert A.adaln_noalloc_read_status() == 0
