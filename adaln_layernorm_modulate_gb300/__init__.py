@@ -31,7 +31,7 @@ EXPORTS = (
     "adaln_fwd_varlen_workspace_size", "adaln_fwd_varlen", "adaln_bwd_varlen_workspace_size",
     "adaln_bwd_varlen", "adaln_bwd_varlen_partials", "adaln_bwd_varlen_reduce",
     "adaln_read_status", "adaln_bwd_recompute_workspace_size", "adaln_bwd_recompute",
-    "adaln_bwd_varlen_recompute_workspace_size", "adaln_bwd_varlen_recompute", "adaln_bwd_noalloc", "adaln_noalloc_read_status",
+    "adaln_bwd_varlen_recompute_workspace_size", "adaln_bwd_varlen_recompute", "adaln_bwd_noalloc", "adaln_noalloc_read_status", "adaln_sum_ranks",
     "adaln_bucket_batch", "adaln_bucket_batch_real",
     "adaln_fit_step_cost", "adaln_bucket_load_cv", "adaln_status_string",
 )
@@ -76,6 +76,7 @@ def _load() -> ctypes.CDLL:
                                         sz, ci, vp], ci),
         "adaln_bwd_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp], ci),
         "adaln_noalloc_read_status": ([vp], ci),
+        "adaln_sum_ranks": ([vp, vp, i32, i64, vp], ci),
         "adaln_bucket_batch": ([i64, i64, i64, i32], i64),
         "adaln_bucket_batch_real": ([i64, i64, i64, ctypes.c_double], i64),
         "adaln_fit_step_cost": ([vp, vp, vp, i64, ctypes.c_double, ctypes.c_double,
@@ -253,6 +254,11 @@ def adaln_bwd_noalloc(dy, x, mean, rstd, scale, dx, dshift, dscale, Bt, N, D, dt
 
 def adaln_noalloc_read_status(stream=None) -> int:
     return int(lib().adaln_noalloc_read_status(_stream(stream)))
+
+
+def adaln_sum_ranks(parts, out, world, n, stream=None):
+    """out[i] = parts[0][i] + ... + parts[world - 1][i], added in rank order (device fp32)."""
+    _check("adaln_sum_ranks", lib().adaln_sum_ranks(_ptr(parts), _ptr(out), world, n, _stream(stream)))
 
 
 def adaln_bucket_batch(S, M_mem, M_comp, p) -> int:

@@ -745,3 +745,17 @@ extern "C" int adaln_noalloc_read_status(cudaStream_t stream) {
     if (int rc = noalloc_scratch(&scratch)) return rc;
     return read_status_words(scratch, stream);
 }
+
+// ---- row sharding across ranks: the fixed-order sum of the gradients --------------------
+
+extern "C" int adaln_sum_ranks(const float* parts, float* out, int32_t world, int64_t n,
+                               cudaStream_t stream) {
+    if (world < 1 || n < 0) return ADALN_ERR_INVALID_ARG;
+    if (n == 0) return ADALN_OK;
+    if (n > INT64_MAX / world) return ADALN_ERR_INVALID_ARG;
+    if (int rc = check_io({parts, out}, {})) return rc;
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    if (sms <= 0) return ADALN_ERR_CUDA;
+    return launched(launch_rank_sum(parts, out, world, n, sms, stream));
+}

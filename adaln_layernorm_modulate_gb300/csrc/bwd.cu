@@ -742,3 +742,47 @@ cudaError_t launch_stage2(const Stage2Args& args, int dtype, bool varlen, int sm
 }
 
 }  // namespace adaln
+
+namespace adaln {
+
+// Sum over ranks of stacked per-rank gradients: out[i] = parts[0][i] + parts[1][i] + ...,
+// always in rank order, so the result depends only on the inputs' bits, not on how they
+// were gathered. 16-byte vectors where n allows, a grid-stride loop.
+__global__ void __launch_bounds__(256) rank_sum_kernel(const float* __restrict__ parts, float* __restrict__ out,
+                                                       int32_t world, int64_t n) {
+    pdl_begin();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (n % 4 == 0) {
+        const int64_t n4 = n / 4;
+        const float4* p4 = reinterpret_cast<const float4*>(parts);
+        float4* o4 = reinterpret_cast<float4*>(out);
+        for (int64_t i = first; i < n4; i += stride) {
+            float4 s = __ldg(p4 + i);
+            for (int32_t r = 1; r < world; ++r) {
+                const float4 v = __ldg(p4 + (int64_t)r * n4 + i);
+                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+            }
+            o4[i] = s;
+        }
+    } else {
+        for (int64_t i = first; i < n; i += stride) {
+            float s = __ldg(parts + i);
+            for (int32_t r = 1; r < world; ++r) s += __ldg(parts + (int64_t)r * n + i);
+            out[i] = s;
+        }
+    }
+}
+
+cudaError_t launch_rank_sum(const float* parts, float* out, int32_t world, int64_t n, int sms,
+                            cudaStream_t stream) {
+    const int64_t units = n % 4 == 0 ? n / 4 : n;
+    int64_t blocks = (units + 255) / 256;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    if (blocks < 1) blocks = 1;
+    void* params[] = {&parts, &out, &world, &n};
+    return launch_dependent(reinterpret_cast<const void*>(&rank_sum_kernel), dim3((unsigned)blocks), dim3(256),
+                            params, 0, stream);
+}
+
+}  // namespace adaln

@@ -27,4 +27,8 @@ cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool
 // Stage 2 of a backward on a device of `sms` multiprocessors.
 cudaError_t launch_stage2(const Stage2Args& args, int dtype, bool varlen, int sms, cudaStream_t stream);
 
+// out[i] = sum over r in rank order of parts[r * n + i].
+cudaError_t launch_rank_sum(const float* parts, float* out, int32_t world, int64_t n, int sms,
+                            cudaStream_t stream);
+
 }  // namespace adaln

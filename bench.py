@@ -63,6 +63,10 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--parallel", choices=["replicas", "shard"], default="replicas",
+                   help="under torchrun: every rank runs the whole batch (replicas), or each rank "
+                        "runs a segment-aligned row shard and the gradients are summed over ranks "
+                        "in rank order (shard)")
     p.add_argument("--max-tokens", type=int, default=0,
                    help="keep only the leading segments holding at most this many tokens "
                         "(a smaller case of the same workload, e.g. for profiler captures)")
@@ -233,12 +237,12 @@ def dist_env():
     return world, rank, local
 
 
-def dist_init(world):
+def dist_init(world, backend="gloo"):
     if world <= 1:
         return None
     import torch.distributed as dist
     os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-    dist.init_process_group("gloo")
+    dist.init_process_group(backend)
     return dist
 
 
@@ -251,7 +255,8 @@ def max_over_ranks(dist, value: float) -> float:
     if dist is None:
         return value
     import torch
-    t = torch.tensor([value], dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -431,11 +436,24 @@ def run_ours(args):
     import adaln_layernorm_modulate_gb300 as A
 
     world, rank, local = dist_env()
-    dist = dist_init(world)
     torch.cuda.set_device(local)
+    # The sharded path's gradient exchange moves device tensors (NCCL); replicas only need a
+    # barrier and a max of times.
+    dist = dist_init(world, "nccl" if args.parallel == "shard" else "gloo")
     dev = torch.device("cuda", local)
 
     w = make_workload(args.workload, bucket_batch=A.adaln_bucket_batch, max_tokens=args.max_tokens)
+    full = w
+    sharded = args.parallel == "shard"
+    if sharded:
+        # This rank's rows: a segment-aligned shard of the batch, as a packed call on its own
+        # segments with the batch's modulation tables.
+        from adaln_layernorm_modulate_gb300 import shard as S
+        sh = S.make_shard(w.cu_seqlens, w.mod_idx, world, rank)
+        w = synth.Workload(name=w.name, seed=w.seed, dtype=w.dtype, D=w.D,
+                           cu_seqlens=sh.cu_seqlens.astype(np.int64), mod_idx=sh.mod_idx.astype(np.int64),
+                           nmod=w.nmod, dense=None, x=w.x[sh.row0:sh.row1], dy=w.dy[sh.row0:sh.row1],
+                           shift=w.shift, scale=w.scale, meta=dict(w.meta))
     e = 2 if w.dtype == synth.BF16 else 4
     tdt = torch.bfloat16 if w.dtype == synth.BF16 else torch.float32
     packed = w.dense is None
@@ -454,8 +472,8 @@ def run_ours(args):
     dx = torch.empty((R, D), dtype=tdt, device=dev)
     mean = torch.empty(R, dtype=torch.float32, device=dev)
     rstd = torch.empty(R, dtype=torch.float32, device=dev)
-    dshift = torch.empty((nmod, D), dtype=torch.float32, device=dev)
-    dscale = torch.empty((nmod, D), dtype=torch.float32, device=dev)
+    grads = torch.empty((2, nmod, D), dtype=torch.float32, device=dev)
+    dshift, dscale = grads[0], grads[1]
     if packed:
         fws_n = A.adaln_fwd_varlen_workspace_size(R, nseg, D, w.dtype)
         bws_n = A.adaln_bwd_varlen_workspace_size(R, nseg, nmod, D, w.dtype)
@@ -510,6 +528,10 @@ def run_ours(args):
         if ev and len(ev) == 4:
             ev[2].record(stream)
         bwd_stage("reduce", d["dy"], d["x"], d["scale"], d["cu"], d["mod"])
+        if sharded and dist is not None:
+            # The one exchange of the sharded path: every rank's gradients, gathered and
+            # summed in rank order (adaln_sum_ranks), the same bits on every rank.
+            S.sum_over_ranks(grads)
         if ev:
             ev[-1].record(stream)
 
@@ -573,7 +595,9 @@ def run_ours(args):
     red_ms = float(np.mean([ev[2].elapsed_time(ev[3]) for ev in split]))
 
     nb = algorithmic_bytes(R, D, e, nmod)
-    value = world * nb["step"] / (ms_per_step / 1e3) / 1e9
+    # Whole-job bytes: every replica's batch, or the one batch the shards split.
+    job_bytes = algorithmic_bytes(full.R, D, e, nmod)["step"] if sharded else world * nb["step"]
+    value = job_bytes / (ms_per_step / 1e3) / 1e9
     peak, peak_src = hbm_peak()
 
     # End to end through the public calls, host buffers in and out, copies inside the region.
@@ -614,25 +638,27 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier(dist)
         e2e_ms = max_over_ranks(dist, a.elapsed_time(b) / args.e2e_steps)
-        e2e = {"value": world * nb["step"] / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+        e2e = {"value": job_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "pipeline": ("%d segment chunks; host-to-device copies, kernels and device-to-host "
                             "copies on three streams" % len(chunks)) if chunks else "serial"}
 
     if rank != 0:
         return 0
-    base = None if args.no_cpu_baseline else cpu_baseline(w, args.cpu_seconds)
+    base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, args.cpu_seconds)
     achieved = nb["bwd_partials"] / (part_ms / 1e3) / 1e9
     traffic = recorded_traffic(w.name)
     lit = world * literal_bytes(R, D, e, nmod)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": describe(w),
+        "scaling": "strong" if sharded else "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": dict(describe(full), parallelism=("row shards (segment-aligned), gradients summed "
+                                                    "over ranks in rank order" if sharded else "replicas")),
         "l2": l2_note,
         "pct_of_peak": 100.0 * value / (world * peak),
-        "mtokens_per_s": world * R / (ms_per_step / 1e3) / 1e6,
+        "mtokens_per_s": (full.R if sharded else world * R) / (ms_per_step / 1e3) / 1e6,
         "literal_bytes": {
             "note": "each tensor of the pass counted once (read x, dy, shift, scale; write y, dx, "
                     "mean, rstd, dshift, dscale); value above counts each call's own traffic",
@@ -649,7 +675,7 @@ def run_ours(args):
                      "algorithmic_bytes": nb["bwd_partials"]},
         "cpu_baseline": base,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (4 if sharded and world > 1 else 3) * args.steps,
         "per_call_note": ("per_call_us and roofline.achieved come from a second pass of the same %d "
                           "steps with CUDA events between the calls; the timed steps record none "
                           "there (each such event costs ~2 us of GPU time)" % args.steps),

@@ -224,6 +224,19 @@ int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean, const fl
  * nothing on the device. Like adaln_bwd_noalloc, this call has no counterpart in the paper. */
 int adaln_noalloc_read_status(cudaStream_t stream);
 
+/* ---- Row sharding across ranks ----------------------------------------------------------
+ * A batch can be split into contiguous, segment-aligned row shards, one per rank (the pages
+ * train on 8- and 16-GPU clusters, AdaptiveLoad technical summary sections 2.A and 4). The
+ * forward needs no exchange; each rank's backward gives dshift/dscale over its own tokens,
+ * and the batch's gradients are their sum over ranks. adaln_sum_ranks forms that sum from
+ * the ranks' fp32 gradients stacked on one device, parts[world][n] (e.g. after an
+ * all-gather), always adding in rank order 0, 1, ..., world - 1:
+ *     out[i] = parts[0][i] + parts[1][i] + ... + parts[world - 1][i]
+ * so every rank that runs it gets the same bits, whatever moved the data. parts and out are
+ * device pointers, 16-byte aligned, not overlapping; n elements each. One launch on
+ * `stream`. Returns ADALN_ERR_INVALID_ARG for world < 1 or n < 0. */
+int adaln_sum_ranks(const float* parts, float* out, int32_t world, int64_t n, cudaStream_t stream);
+
 /* Dual-constraint bucket size, AdaptiveLoad technical summary section 2.A:
  *     B = max(1, min(floor(M_mem / S), floor(M_comp / S^p)))
  * with exact integer arithmetic (S^p is never formed past M_comp). Host only.
