@@ -105,9 +105,11 @@ enum Kind { kFwd = 0, kBwd = 1 };
 // SM. A CTA alone on its SM (wide rows in the backward) stops at 150 KB: deeper rings
 // measured slower, the rest of the SM's shared memory serving as L1.
 constexpr size_t kRingBudget = 150 * 1024;
-// Rows whose two-round ring exceeds the budget still get one, up to this size (fp32
-// D=12288 backward: two rounds of 96 KB), rather than plain loads into registers.
-constexpr size_t kRingLimit = 200 * 1024;
+// Rows whose two-round ring exceeds the budget still get one, up to this size, rather than
+// plain loads into registers (fp32 D=12288 backward: two rounds of 96 KB; fp32 D=14336: two
+// rounds of 112 KB, 1355 -> 868 us against plain loads). With the kernels' static shared
+// memory (about 0.5 KB for such wide rows) it stays within the 227 KB a CTA may opt into.
+constexpr size_t kRingLimit = 226 * 1024;
 // Forwards with at least this many rows per resident CTA slot of the bulk-ring plan stage
 // rows with the per-thread copy ring where copy_ring_cfg allows it, shorter ones with the
 // bulk ring (which starts faster, see fwd.cu). bf16 D=3072 (912 bulk-ring slots on 152

@@ -83,6 +83,8 @@ SMALL = {
     "dense-bf16-1x37x14336": lambda: synth.dense("c", 122, synth.BF16, 1, 37, 14336, dy_std=0.1),
     "packed-bf16-d10240": lambda: synth.make("c", 123, synth.BF16, 10240, [20, 1, 25], [0, 1, 0], 2,
                                              x_mode=synth.ROWS_SCALED, dy_std=0.02),
+    # fp32 D=14336: a two-round backward ring of 224 KB, near the per-CTA shared-memory limit.
+    "dense-f32-2x19x14336": lambda: synth.dense("c", 124, synth.F32, 2, 19, 14336, dy_std=0.1),
     # Rows too wide for a two-round backward ring: plain loads, x and dy read twice.
     "dense-f32-2x21x16384": lambda: synth.dense("c", 119, synth.F32, 2, 21, 16384, dy_std=0.1),
     "packed-f32-d128-many": lambda: synth.make(
