@@ -515,18 +515,23 @@ def run_ours(args):
                w.dtype, sptr)
 
     def step(ev):
-        # ev: None (no events), [begin, end], or [begin, after fwd, after partials, end]. An
-        # event recorded between two launches costs about 2 us of GPU time on GB300, so the
-        # headline steps record none between their calls; a second pass times each call.
+        # ev: None (no events), [begin, end], [begin, after fwd, after partials, end], or, when
+        # each timed call gets its own L2 flush, [begin, after fwd, after the flush, after
+        # partials, end]. An event recorded between two launches costs about 2 us of GPU time
+        # on GB300, so the headline steps record none between their calls; a second pass times
+        # each call.
         shape_batch()
         if ev:
             ev[0].record(stream)
         fwd(d["x"], d["shift"], d["scale"], d["cu"], d["mod"])
-        if ev and len(ev) == 4:
+        if ev and len(ev) >= 4:
             ev[1].record(stream)
-        bwd_stage("partials", d["dy"], d["x"], d["scale"], d["cu"], d["mod"])
-        if ev and len(ev) == 4:
+        if ev and len(ev) == 5:
+            torch.sum(flush, dim=0, out=flush_sum)
             ev[2].record(stream)
+        bwd_stage("partials", d["dy"], d["x"], d["scale"], d["cu"], d["mod"])
+        if ev and len(ev) >= 4:
+            ev[-2].record(stream)
         bwd_stage("reduce", d["dy"], d["x"], d["scale"], d["cu"], d["mod"])
         if sharded and dist is not None:
             # The one exchange of the sharded path: every rank's gradients, gathered and
@@ -587,12 +592,14 @@ def run_ours(args):
         step_ms = float(np.mean([ev[0].elapsed_time(ev[1]) for ev in step_events]))
     ms_per_step = max_over_ranks(dist, step_ms)
     # The per-call breakdown (and the roofline's kernel time): the same K steps again with
-    # events between the calls.
-    _, _, split = run_steps(lambda: events(4))
+    # events between the calls. Where the activations fit in L2 the backward also gets its
+    # own flush (a read, outside its events), as each timed call does: otherwise the
+    # forward's output, still dirty in L2, would be written back inside the backward's time.
+    _, _, split = run_steps(lambda: events(5 if flush is not None else 4))
     clk = clocks.stop()
     fwd_ms = float(np.mean([ev[0].elapsed_time(ev[1]) for ev in split]))
-    part_ms = float(np.mean([ev[1].elapsed_time(ev[2]) for ev in split]))
-    red_ms = float(np.mean([ev[2].elapsed_time(ev[3]) for ev in split]))
+    part_ms = float(np.mean([ev[-3].elapsed_time(ev[-2]) for ev in split]))
+    red_ms = float(np.mean([ev[-2].elapsed_time(ev[-1]) for ev in split]))
 
     nb = algorithmic_bytes(R, D, e, nmod)
     # Whole-job bytes: every replica's batch, or the one batch the shards split.
@@ -677,8 +684,10 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": (4 if sharded and world > 1 else 3) * args.steps,
         "per_call_note": ("per_call_us and roofline.achieved come from a second pass of the same %d "
-                          "steps with CUDA events between the calls; the timed steps record none "
-                          "there (each such event costs ~2 us of GPU time)" % args.steps),
+                          "steps with CUDA events between the calls%s; the timed steps record none "
+                          "there (each such event costs ~2 us of GPU time)"
+                          % (args.steps, ", and an L2 flush before the backward as before the forward"
+                             if flush is not None else "")),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
