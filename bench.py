@@ -9,9 +9,12 @@ tokens); its activations (3.3 GB per tensor) are far larger than L2, so no flush
 needed between steps.
 
 Prints ONE JSON line (rank 0). `value` is algorithmic HBM bytes of forward + backward
-divided by the device time of a step (GB/s), summed over ranks; under torchrun every
-rank runs an independent replica (the path needs no collective to shard across
-replicas). `--impl reference` times the CPU oracle instead, on a bounded sample.
+divided by the device time of a step (GB/s), over the whole job. Under torchrun every rank
+runs an independent replica by default (value summed over ranks, weak scaling); with
+`--parallel shard` the ranks split one batch into segment-aligned row shards and each step
+ends with the one exchange the path has, the rank-order sum of the modulation gradients
+(value = the batch's bytes over the slowest rank's step, strong scaling). `--impl
+reference` times the CPU oracle instead, on a bounded sample.
 """
 from __future__ import annotations
 
