@@ -362,74 +362,90 @@ def chunked_e2e_step(A, w, chunks, pin, out_h, d, outs, sptr, shape_batch, dev):
     """One end-to-end step over segment chunks: chunk c's inputs go up on a copy stream, its
     forward and backward run on the compute stream once they have landed, and its outputs
     come down on a third stream, so copies in both directions overlap the kernels and each
-    other. Each chunk is a packed call on its own segments and table rows."""
+    other. Each chunk is a packed call on its own segments and table rows. Consecutive steps
+    alternate between two sets of device buffers (inputs, tables, outputs), so a step's
+    inputs go up while the step before it is still computing and copying its results down;
+    a set is refilled only once the step that last used it has read its inputs and copied
+    its outputs down. `step.finish()` makes the compute stream wait for every copy issued."""
     import torch
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     cu = np.asarray(w.cu_seqlens)
-    plan = []
-    ws_f = ws_b = 0
-    for s0, s1 in chunks:
-        t0, t1 = int(cu[s0]), int(cu[s1])
-        local_cu = torch.from_numpy((cu[s0:s1 + 1] - t0).astype(np.int32)).pin_memory()
-        local_mod = torch.from_numpy(np.arange(s1 - s0, dtype=np.int32)).pin_memory()
-        R, nseg = t1 - t0, s1 - s0
-        ws_f = max(ws_f, A.adaln_fwd_varlen_workspace_size(R, nseg, w.D, w.dtype))
-        ws_b = max(ws_b, A.adaln_bwd_varlen_workspace_size(R, nseg, nseg, w.D, w.dtype))
-        plan.append((s0, s1, t0, t1, local_cu, local_mod,
-                     torch.empty(s1 - s0 + 1, dtype=torch.int32, device=dev),
-                     torch.empty(s1 - s0, dtype=torch.int32, device=dev)))
-    wsf = torch.empty(ws_f, dtype=torch.uint8, device=dev)
-    wsb = torch.empty(ws_b, dtype=torch.uint8, device=dev)
     rows = ("x", "dy")
     tables = ("shift", "scale")
     out_rows = ("y", "dx", "mean", "rstd")
     out_tables = ("dshift", "dscale")
-    state = {"last_compute": None, "last_out": None}
+    host_tables = []
+    ws_f = ws_b = 0
+    for s0, s1 in chunks:
+        t0, t1 = int(cu[s0]), int(cu[s1])
+        host_tables.append((torch.from_numpy((cu[s0:s1 + 1] - t0).astype(np.int32)).pin_memory(),
+                            torch.from_numpy(np.arange(s1 - s0, dtype=np.int32)).pin_memory()))
+        R, nseg = t1 - t0, s1 - s0
+        ws_f = max(ws_f, A.adaln_fwd_varlen_workspace_size(R, nseg, w.D, w.dtype))
+        ws_b = max(ws_b, A.adaln_bwd_varlen_workspace_size(R, nseg, nseg, w.D, w.dtype))
+    wsf = torch.empty(ws_f, dtype=torch.uint8, device=dev)  # compute-stream order: one suffices
+    wsb = torch.empty(ws_b, dtype=torch.uint8, device=dev)
+
+    def buffer_set(dd, oo):
+        tabs = [(torch.empty(hc.numel(), dtype=torch.int32, device=dev),
+                 torch.empty(hm.numel(), dtype=torch.int32, device=dev)) for hc, hm in host_tables]
+        return {"d": dd, "o": oo, "tables": tabs, "read": None, "written": None}
+
+    sets = [buffer_set(d, outs),
+            buffer_set({k: torch.empty_like(d[k]) for k in rows + tables},
+                       {k: torch.empty_like(v) for k, v in outs.items()})]
+    state = {"k": 0}
 
     def step():
         shape_batch()
-        begin = torch.cuda.Event()
-        begin.record(comp)
-        s_in.wait_event(begin)  # nothing of this step starts before what precedes it on comp
-        if state["last_compute"] is not None:
-            s_in.wait_event(state["last_compute"])  # inputs are overwritten only once read
-            comp.wait_event(state["last_out"])      # outputs only once copied down
-        for s0, s1, t0, t1, hcu, hmod, dcu, dmod in plan:
+        bs = sets[state["k"] % 2]
+        state["k"] += 1
+        if bs["read"] is not None:
+            s_in.wait_event(bs["read"])      # this set's inputs are no longer read
+            comp.wait_event(bs["written"])   # its outputs have been copied down
+        dd, oo = bs["d"], bs["o"]
+        for (s0, s1), (hcu, hmod), (dcu, dmod) in zip(chunks, host_tables, bs["tables"]):
+            t0, t1 = int(cu[s0]), int(cu[s1])
             with torch.cuda.stream(s_in):
                 for k in rows:
-                    d[k][t0:t1].copy_(pin[k][t0:t1], non_blocking=True)
+                    dd[k][t0:t1].copy_(pin[k][t0:t1], non_blocking=True)
                 for k in tables:
-                    d[k][s0:s1].copy_(pin[k][s0:s1], non_blocking=True)
+                    dd[k][s0:s1].copy_(pin[k][s0:s1], non_blocking=True)
                 dcu.copy_(hcu, non_blocking=True)
                 dmod.copy_(hmod, non_blocking=True)
                 landed = torch.cuda.Event()
                 landed.record(s_in)
             comp.wait_event(landed)
             R, nseg = t1 - t0, s1 - s0
-            A.adaln_fwd_varlen(d["x"][t0:t1], d["shift"][s0:s1], d["scale"][s0:s1], outs["y"][t0:t1],
-                               outs["mean"][t0:t1], outs["rstd"][t0:t1], dcu, dmod, nseg, R, nseg, w.D,
+            A.adaln_fwd_varlen(dd["x"][t0:t1], dd["shift"][s0:s1], dd["scale"][s0:s1], oo["y"][t0:t1],
+                               oo["mean"][t0:t1], oo["rstd"][t0:t1], dcu, dmod, nseg, R, nseg, w.D,
                                EPS, wsf, ws_f, w.dtype, sptr)
-            A.adaln_bwd_varlen(d["dy"][t0:t1], d["x"][t0:t1], outs["mean"][t0:t1], outs["rstd"][t0:t1],
-                               d["scale"][s0:s1], outs["dx"][t0:t1], outs["dshift"][s0:s1],
-                               outs["dscale"][s0:s1], dcu, dmod, nseg, R, nseg, w.D, wsb, ws_b,
+            A.adaln_bwd_varlen(dd["dy"][t0:t1], dd["x"][t0:t1], oo["mean"][t0:t1], oo["rstd"][t0:t1],
+                               dd["scale"][s0:s1], oo["dx"][t0:t1], oo["dshift"][s0:s1],
+                               oo["dscale"][s0:s1], dcu, dmod, nseg, R, nseg, w.D, wsb, ws_b,
                                w.dtype, sptr)
             done = torch.cuda.Event()
             done.record(comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(done)
                 for k in out_rows:
-                    out_h[k][t0:t1].copy_(outs[k][t0:t1], non_blocking=True)
+                    out_h[k][t0:t1].copy_(oo[k][t0:t1], non_blocking=True)
                 for k in out_tables:
-                    out_h[k][s0:s1].copy_(outs[k][s0:s1], non_blocking=True)
-        state["last_compute"] = torch.cuda.Event()
-        state["last_compute"].record(comp)
-        state["last_out"] = torch.cuda.Event()
-        state["last_out"].record(s_out)
-        comp.wait_event(state["last_out"])  # the step ends when its last copy has landed
+                    out_h[k][s0:s1].copy_(oo[k][s0:s1], non_blocking=True)
+        bs["read"] = torch.cuda.Event()
+        bs["read"].record(comp)
+        bs["written"] = torch.cuda.Event()
+        bs["written"].record(s_out)
 
+    def finish():
+        for bs in sets:
+            if bs["written"] is not None:
+                comp.wait_event(bs["written"])
+
+    step.finish = finish
     step.h2d_bytes = sum(pin[k].element_size() * pin[k].numel() for k in rows + tables) + sum(
-        (c[4].numel() + c[5].numel()) * 4 for c in plan)
+        (hc.numel() + hm.numel()) * 4 for hc, hm in host_tables)
     return step
 
 
@@ -638,12 +654,17 @@ def run_ours(args):
             e2e_step = chunked_e2e_step(A, w, chunks, pin, out_h, d, outs, sptr, shape_batch, dev)
             h2d = e2e_step.h2d_bytes
         e2e_step()
+        if chunks is not None:
+            e2e_step()  # both buffer sets warmed up
+            e2e_step.finish()
         torch.cuda.synchronize()
         a, b = events(2)
         barrier(dist)
         a.record(stream)
         for _ in range(args.e2e_steps):
             e2e_step()
+        if chunks is not None:
+            e2e_step.finish()  # the region ends when the last copy has landed
         b.record(stream)
         torch.cuda.synchronize()
         barrier(dist)
@@ -651,7 +672,8 @@ def run_ours(args):
         e2e = {"value": job_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "pipeline": ("%d segment chunks; host-to-device copies, kernels and device-to-host "
-                            "copies on three streams" % len(chunks)) if chunks else "serial"}
+                            "copies on three streams, two buffer sets alternating between steps"
+                            % len(chunks)) if chunks else "serial"}
 
     if rank != 0:
         return 0

@@ -1,5 +1,5 @@
 """The pipelined end-to-end step of bench.py (segment chunks on copy-in, compute and
-copy-out streams) gives bitwise the results of the same chunk calls made one after another
+copy-out streams, two device buffer sets alternating between steps) gives bitwise the results of the same chunk calls made one after another
 on one stream (so no copy overtakes a launch that needs it), and the whole-batch call's
 results within rounding: a chunk's forward may map its rows differently from the whole
 batch's (tile length decides between the two forward stagings for some bf16 widths), which
@@ -40,8 +40,9 @@ def test_chunked_end_to_end_step_matches_whole_batch_calls():
     assert chunks is not None and len(chunks) > 2
     sptr = torch.cuda.current_stream().cuda_stream
     step = bench.chunked_e2e_step(A, w, chunks, pin, out_h, d, outs, sptr, lambda: None, dev)
-    step()
-    step()
+    for _ in range(3):  # both buffer sets, then the first one refilled
+        step()
+    step.finish()
     torch.cuda.synchronize()
 
     cu = np.asarray(w.cu_seqlens)
