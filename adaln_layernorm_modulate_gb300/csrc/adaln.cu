@@ -90,6 +90,12 @@ RowCfg row_cfg(int64_t D, adaln_dtype dtype, bool forward) {
         if (best == 0 || std::llabs(nv - target) < std::llabs(best - target)) best = nv;
     }
     if (best != 0) return RowCfg{best, (int)(V / best), true};
+    // bf16 backward rows too wide for four vectors a thread within max_threads(4, 8): the
+    // wide form, four vectors a thread over up to kWideThreads threads, x and dy read from the
+    // ring twice (D=14336: 448 threads; D=16384: 512).
+    if (!forward && bf16 && V % 4 == 0 && (V / 4) % 32 == 0 && V / 4 > max_threads(4, (int)VE) &&
+        V / 4 <= kWideThreads)
+        return RowCfg{4, (int)(V / 4), true};
     for (int nv : kNv) {
         if (nv < target) continue;
         const int64_t tpb = ((V + nv - 1) / nv + 31) / 32 * 32;

@@ -21,15 +21,18 @@
 
 namespace adaln {
 
-template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
-__global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) bwd_kernel(const BwdArgs a) {
+// WIDE: bf16 rows of four vectors a thread over more than max_threads(4, 8) threads (D of
+// 14336 and 16384: 448 and 512 threads), which read x and dy from the ring twice so that only
+// the column accumulators and (1 + scale) stay in registers (128 a thread at 512).
+template <typename T, int NV, bool VARLEN, bool RING, bool FULL, bool WIDE = false>
+__global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::VE)) bwd_kernel(const BwdArgs a) {
     pdl_begin();
     using IO = Io<T>;
     constexpr int VE = IO::VE;
     constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector
     constexpr int RB = RowShape<NV>::kRows;
     // Wide rows read x and dy from the ring twice instead of holding them in registers.
-    constexpr bool REREAD = RING && NV >= 6;
+    constexpr bool REREAD = RING && (NV >= 6 || WIDE);
     static_assert(!REREAD || RB == 1, "wide rows are staged one a round");
     extern __shared__ uint4 ring[];
     __shared__ __align__(16) float red[2][2 * RB][32];  // double-buffered per-warp sums of g, g*xhat
@@ -659,9 +662,9 @@ __global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2A
     }
 }
 
-template <typename T, int NV, bool VARLEN, bool RING, bool FULL>
+template <typename T, int NV, bool VARLEN, bool RING, bool FULL, bool WIDE = false>
 static const void* bwd_fn() {
-    return reinterpret_cast<const void*>(&bwd_kernel<T, NV, VARLEN, RING, FULL>);
+    return reinterpret_cast<const void*>(&bwd_kernel<T, NV, VARLEN, RING, FULL, WIDE>);
 }
 
 // Instantiated variants: ring + full row, ring + partial row, plain (partial row).
@@ -684,7 +687,12 @@ static const void* pick_nv(int nv, bool ring, bool full) {
     }
 }
 
-static const void* pick_bwd(int dtype, int nv, bool varlen, bool ring, bool full) {
+static const void* pick_bwd(int dtype, int nv, bool varlen, bool ring, bool full, int tpb) {
+    if (dtype == 1 && nv == 4 && tpb > max_threads(4, 8)) {  // the wide form: ring, full rows
+        if (!ring || !full || tpb > kWideThreads) return nullptr;
+        return varlen ? bwd_fn<__nv_bfloat16, 4, true, true, true, true>()
+                      : bwd_fn<__nv_bfloat16, 4, false, true, true, true>();
+    }
     if (dtype == 0) return varlen ? pick_nv<float, true>(nv, ring, full) : pick_nv<float, false>(nv, ring, full);
     if (dtype == 1)
         return varlen ? pick_nv<__nv_bfloat16, true>(nv, ring, full)
@@ -694,7 +702,7 @@ static const void* pick_bwd(int dtype, int nv, bool varlen, bool ring, bool full
 
 cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
                               size_t smem, int* out) {
-    const void* fn = pick_bwd(dtype, nv, varlen, ring, full);
+    const void* fn = pick_bwd(dtype, nv, varlen, ring, full, tpb);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = allow_dynamic_smem(fn);
     if (e != cudaSuccess) return e;
@@ -703,7 +711,7 @@ cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool fu
 
 cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
                        int64_t G, int tpb, size_t smem, cudaStream_t stream) {
-    const void* fn = pick_bwd(dtype, nv, varlen, ring, full);
+    const void* fn = pick_bwd(dtype, nv, varlen, ring, full, tpb);
     if (!fn) return cudaErrorInvalidValue;
     BwdArgs a = args;
     void* params[] = {&a};

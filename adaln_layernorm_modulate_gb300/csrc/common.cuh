@@ -20,6 +20,9 @@ enum : int { kRingNone = 0, kRingBulk = 1, kRingCopy = 2 };  // forward staging 
 __host__ __device__ constexpr int max_threads(int nv, int ve) {
     return nv == 1 ? 512 : nv >= 8 ? (ve == 8 ? 256 : 512) : 384;
 }
+// Launch bound of the backward's wide form (bf16, four vectors a thread, more threads than
+// max_threads(4, 8)): the row's x and dy are read from the ring twice.
+constexpr int kWideThreads = 512;
 
 // A CTA processes its rows in rounds of kRows rows, each thread owning NV 16-byte column
 // vectors of every row. Wider per-thread slices hold fewer rows per round so the values
