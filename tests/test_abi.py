@@ -96,6 +96,13 @@ def test_argument_checks_before_any_device_work():
     assert L.adaln_fwd_varlen(16, 16, 16, 16, 16, 16, 16, 16, 1, 5, 1, 64, 1e-6, 256, 16, 1, None) == 4
     assert L.adaln_bwd_varlen(16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 5, 1, 64, None, 0, 1, None) == 4
     assert L.adaln_read_status(None, None) == 4
+    # rank-order gradient sum: world, size, pointers
+    assert L.adaln_sum_ranks(16, 32, 0, 8, None) == 1
+    assert L.adaln_sum_ranks(16, 32, 2, -1, None) == 1
+    assert L.adaln_sum_ranks(16, 32, 2, 0, None) == 0
+    assert L.adaln_sum_ranks(None, 32, 2, 8, None) == 1
+    assert L.adaln_sum_ranks(16, 40, 2, 8, None) == 3
+    assert L.adaln_sum_ranks(16, 32, 2, 2 ** 62, None) == 1
 
 
 def test_workspace_size_rejects_bad_shapes():

@@ -91,6 +91,15 @@ SMALL = {
         "c", 111, synth.F32, 128, list(np.random.default_rng(5).integers(0, 10, 100)),
         list(np.random.default_rng(6).integers(0, 13, 100)), 13),
     "dense-f32-one-row": lambda: synth.dense("c", 112, synth.F32, 1, 1, 1536),
+    # Many short samples: few pieces per modulation row, so row-major partials and the
+    # row-major stage 2 of a dense batch.
+    "dense-bf16-800x5x1024": lambda: synth.dense("c", 125, synth.BF16, 800, 5, 1024,
+                                                 x_mode=synth.ROWS_SCALED, dy_std=0.02),
+    # The backward's wide form (bf16 D=16384, 4 x 512 threads) on a packed table whose
+    # modulation rows are shared and whose segments end inside tiles.
+    "packed-bf16-d16384-wide": lambda: synth.make("c", 126, synth.BF16, 16384, [30, 2, 9, 0, 41],
+                                                  [1, 0, 1, 2, 0], 3, x_mode=synth.ROWS_SCALED,
+                                                  dy_std=0.02),
     # More segments than stage 2 examines in one pass of the table (1024), rows of the
     # modulation table whose segments fall in several passes, and empty segments.
     "packed-f32-d64-3000seg": lambda: synth.make(
