@@ -595,7 +595,7 @@ def run_ours(args):
     else:
         l2_note = "activations larger than L2 (%.2f GB per tensor); no flush" % (tensor_bytes / 1e9)
 
-    def run_steps(per_step):
+    def run_steps(per_step, flushed=True):
         # K steps, each preceded by the L2 flush when there is one (outside its events).
         step_events = [per_step() for _ in range(args.steps)]
         t0, t1 = events(2)
@@ -603,7 +603,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0.record(stream)
         for ev in step_events:
-            if flush is not None:
+            if flush is not None and flushed:
                 torch.sum(flush, dim=0, out=flush_sum)
             step(ev)
         t1.record(stream)
@@ -625,6 +625,13 @@ def run_ours(args):
     # own flush (a read, outside its events), as each timed call does: otherwise the
     # forward's output, still dirty in L2, would be written back inside the backward's time.
     _, _, split = run_steps(lambda: events(5 if flush is not None else 4))
+    # Where the steps are flushed, also the steady back-to-back rate without the flush (each
+    # step then also writes back the previous step's outputs left dirty in L2): a secondary
+    # figure.
+    steady = None
+    if flush is not None:
+        s0, s1, _ = run_steps(lambda: None, flushed=False)
+        steady_ms = max_over_ranks(dist, s0.elapsed_time(s1) / args.steps)
     clk = clocks.stop()
     fwd_ms = float(np.mean([ev[0].elapsed_time(ev[1]) for ev in split]))
     part_ms = float(np.mean([ev[-3].elapsed_time(ev[-2]) for ev in split]))
@@ -634,7 +641,14 @@ def run_ours(args):
     # Whole-job bytes: every replica's batch, or the one batch the shards split.
     job_bytes = algorithmic_bytes(full.R, D, e, nmod)["step"] if sharded else world * nb["step"]
     value = job_bytes / (ms_per_step / 1e3) / 1e9
+    if flush is not None:
+        steady = {"note": "back-to-back steps without the L2 flush: each step also writes back the "
+                          "previous step's outputs still dirty in L2, which the flushed figure above "
+                          "leaves to the flush outside its timed region",
+                  "ms_per_step": steady_ms, "value": job_bytes / (steady_ms / 1e3) / 1e9, "unit": "GB/s"}
     peak, peak_src = hbm_peak()
+    if steady is not None:
+        steady["pct_of_peak"] = 100.0 * steady["value"] / (world * peak)
 
     # End to end through the public calls, host buffers in and out, copies inside the region.
     e2e = None
@@ -701,6 +715,7 @@ def run_ours(args):
         "l2": l2_note,
         "pct_of_peak": 100.0 * value / (world * peak),
         "mtokens_per_s": (full.R if sharded else world * R) / (ms_per_step / 1e3) / 1e6,
+        "steady_no_flush": steady,
         "literal_bytes": {
             "note": "each tensor of the pass counted once (read x, dy, shift, scale; write y, dx, "
                     "mean, rstd, dshift, dscale); value above counts each call's own traffic",
