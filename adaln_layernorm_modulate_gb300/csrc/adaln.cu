@@ -128,8 +128,9 @@ struct Plan {
     bool full;      // ring kernel specialised for rows the CTA covers exactly
     int stages;     // ring depth in rounds
     size_t smem;    // dynamic shared memory per CTA
-    int64_t G;      // row tiles = CTAs
+    int64_t G;      // CTAs (= row tiles, or twice the row tiles in the split form)
     int sms;
+    bool split;     // the backward's split form: two-CTA clusters, half a row each
 };
 
 // One ring round: RB rows of x (and of dy for the backward), each padded to the CTA's
@@ -191,6 +192,44 @@ bool ring_shape(Kind kind, adaln_dtype dtype, bool varlen, int dev, Plan* p) {
     return true;
 }
 
+// The backward's split form for fp32 rows too wide for a two-round ring: a cluster of two
+// CTAs per row tile, each staging half of every row (eight vectors a thread) in a ring of as
+// many rounds as kRingLimit holds (three at D=16384: 3 x 64 KB), one cluster per resident
+// cluster slot (cached per device).
+bool split_plan(int64_t D, bool varlen, int dev, int64_t R, Plan* p) {
+    const int64_t VC = D / 4 / 2;  // fp32 vectors of half a row
+    const int tpb = (int)(((VC + 7) / 8 + 31) / 32 * 32);
+    if (tpb > kSplitThreads) return false;
+    p->c = RowCfg{8, tpb, VC == 8 * (int64_t)tpb};
+    p->ring = kRingBulk;
+    p->full = p->c.full;
+    p->split = true;
+    const size_t round = ring_round_bytes(kBwd, p->c, kRingBulk);
+    const size_t st = std::min<size_t>(kMaxStages, (kRingLimit - kRingHeader) / round);
+    if (st < 2) return false;
+    p->stages = (int)st;
+    p->smem = kRingHeader + st * round;
+    const auto key = std::make_tuple(dev, (int)kBwd, (int)ADALN_F32, 8, 32 + (int)varlen * 2 + (int)p->full,
+                                     tpb);
+    int clusters = 0;  // resident clusters on the device
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) clusters = it->second.second;
+    }
+    if (clusters == 0) {
+        if (bwd_split_clusters(varlen, p->full, tpb, p->smem, &clusters) != cudaSuccess || clusters <= 0)
+            return false;
+        std::lock_guard<std::mutex> lock(g_mu);
+        g_plans[key] = {p->stages, clusters};
+    }
+    int64_t tiles = std::min<int64_t>(clusters, kMaxCtas / 2);
+    if (tiles > R) tiles = R;
+    if (tiles < 1) tiles = 1;
+    p->G = 2 * tiles;
+    return true;
+}
+
 // Launch plan: staging mode, ring depth, and row tiles = every resident CTA slot of the
 // device (at most one per row).
 bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, Plan* p) {
@@ -198,9 +237,13 @@ bool make_plan(Kind kind, adaln_dtype dtype, int64_t D, bool varlen, int64_t R, 
     const int sms = current_sms(&dev);
     if (sms <= 0) return false;
     p->sms = sms;
+    p->split = false;
     p->c = row_cfg(D, dtype, kind == kFwd);
-    // A ring needs two rounds; rows too wide for two rounds in kRingLimit load into registers.
+    // A ring needs two rounds; rows too wide for two rounds in kRingLimit load into registers,
+    // except fp32 backward rows, which take the split form.
     p->ring = 2 * ring_round_bytes(kind, p->c, kRingBulk) + kRingHeader <= kRingLimit ? kRingBulk : kRingNone;
+    if (kind == kBwd && p->ring == kRingNone && dtype == ADALN_F32 && split_plan(D, varlen, dev, R, p))
+        return true;
     p->full = p->ring && p->c.full;
     if (!ring_shape(kind, dtype, varlen, dev, p)) return false;
     RowCfg copy;
@@ -361,6 +404,7 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
     Plan p;
     if (!make_plan(kBwd, dtype, D, varlen, seg.R, &p)) return ADALN_ERR_CUDA;
     const int64_t G = p.G;
+    const int64_t tiles = p.split ? G / 2 : G;
     if (int rc = check_workspace(ws, ws_bytes, bwd_need(G, seg.nseg, D))) return rc;
     char* base = static_cast<char*>(ws);
     BwdArgs a{};
@@ -371,7 +415,7 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
     a.scale = scale;
     a.dx = dx;
     a.partials = reinterpret_cast<float*>(base + kPartialsOffset);
-    const int64_t per_row = pieces_per_row(G, seg.nseg, seg.nmod);
+    const int64_t per_row = pieces_per_row(tiles, seg.nseg, seg.nmod);
     a.vec_major = per_row >= kVecMajorPieces ? 1 : 0;
     a.D = D;
     a.seg = seg;
@@ -380,7 +424,7 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
     a.stages = p.stages;
     if (stages & kPartials) {
         if (int rc = launched(launch_bwd(a, (int)dtype, p.c.nv, varlen, p.ring != kRingNone, p.full, G, p.c.tpb,
-                                         p.smem, stream)))
+                                         p.smem, p.split, stream)))
             return rc;
     }
     if (!(stages & kReduce) || seg.nmod == 0) return ADALN_OK;
@@ -389,8 +433,8 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
     s.dshift = dshift;
     s.dscale = dscale;
     s.D = D;
-    s.G = G;
-    s.S = G + seg.nseg;
+    s.G = tiles;
+    s.S = tiles + seg.nseg;
     s.vec_major = a.vec_major;
     s.cw = stage2_cw(D, seg.nmod, p.sms);
     s.splits = stage2_splits(per_row);

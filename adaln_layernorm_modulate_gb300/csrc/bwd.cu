@@ -24,16 +24,22 @@ namespace adaln {
 // WIDE: bf16 rows of four vectors a thread over more than max_threads(4, 8) threads (D of
 // 14336 and 16384: 448 and 512 threads), which read x and dy from the ring twice so that only
 // the column accumulators and (1 + scale) stay in registers (128 a thread at 512).
-template <typename T, int NV, bool VARLEN, bool RING, bool FULL, bool WIDE = false>
-__global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::VE)) bwd_kernel(const BwdArgs a) {
+// SPLIT: fp32 rows too wide for a ring of two rounds (D > 14456). The grid is made of
+// two-CTA clusters, a cluster per row tile; CTA r of a cluster stages and owns half r of
+// every row (a ring of half rows), and the two CTAs add their row sums of g and g*xhat after
+// exchanging them through distributed shared memory (the same bits in both).
+template <typename T, int NV, bool VARLEN, bool RING, bool FULL, bool WIDE = false, bool SPLIT = false>
+__global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : max_threads(NV, Io<T>::VE))
+    bwd_kernel(const BwdArgs a) {
     pdl_begin();
     using IO = Io<T>;
     constexpr int VE = IO::VE;
     constexpr int PV = VE / 2;  // fp32 pairs per 16-byte vector
     constexpr int RB = RowShape<NV>::kRows;
     // Wide rows read x and dy from the ring twice instead of holding them in registers.
-    constexpr bool REREAD = RING && (NV >= 6 || WIDE);
+    constexpr bool REREAD = RING && (NV >= 6 || WIDE) && !SPLIT;
     static_assert(!REREAD || RB == 1, "wide rows are staged one a round");
+    static_assert(!SPLIT || (RING && !WIDE), "the split form stages half rows in a ring");
     extern __shared__ uint4 ring[];
     __shared__ __align__(16) float red[2][2 * RB][32];  // double-buffered per-warp sums of g, g*xhat
 
@@ -42,8 +48,13 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::V
     const int nwarps = TPB >> 5;
     int ng = 1;  // warps rounded up to a power of two
     while (ng < nwarps) ng <<= 1;
-    const int64_t G = gridDim.x, b = blockIdx.x;
+    // Row tiles: one per CTA, or per cluster in the split form (CTA `half` of it covering
+    // vectors half * VC .. half * VC + VC - 1 of every row).
+    const uint32_t half = SPLIT ? cluster_ctarank() : 0u;
+    const int64_t G = SPLIT ? gridDim.x / 2 : gridDim.x, b = SPLIT ? blockIdx.x / 2 : blockIdx.x;
     const int64_t R = a.seg.R, D = a.D, V = D / VE;
+    const int64_t VC = SPLIT ? V / 2 : V;
+    const uint32_t copy_off = (uint32_t)((int64_t)half * VC * 16), copy_bytes = (uint32_t)(VC * 16);
     const int64_t r0 = tile_begin(b, R, G), r1 = tile_begin(b + 1, R, G);
     const char* __restrict__ xb = static_cast<const char*>(a.x);
     const char* __restrict__ gb = static_cast<const char*>(a.dy);
@@ -55,6 +66,9 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::V
     // Ring layout (32-bit shared addresses): ns mbarriers (first 128 bytes), then [ns][RB]
     // row pairs (x, dy), each row at the offsets it has in global memory.
     __shared__ int abort_flag;
+    // Split form: the peer CTA's row sums (double-buffered by round) and their mbarriers.
+    __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ float xch[2][2 * RB];
     const uint32_t vk = (uint32_t)TPB * 16u;
     const uint32_t vrow = (uint32_t)NV * vk;           // one tensor's row slot
     const uint32_t vslot = (uint32_t)RB * 2u * vrow;   // one round: RB rows of x and dy
@@ -68,10 +82,18 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::V
     if constexpr (RING) {
         if (tid == 0) {
             for (int q = 0; q < ns; ++q) mbar_init(bars + 8u * q, 1);
+            if constexpr (SPLIT) {
+                mbar_init(smem_addr(&xbar[0]), 1);
+                mbar_init(smem_addr(&xbar[1]), 1);
+            }
             abort_flag = 0;
             mbar_fence_init();
         }
-        __syncthreads();
+        // The split form: the peer's barriers are initialised before either CTA arrives on them.
+        if constexpr (SPLIT)
+            cluster_sync();
+        else
+            __syncthreads();
     }
 
     uint32_t colb[NV];
@@ -79,8 +101,13 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::V
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         const int64_t v = tid + (int64_t)k * TPB;
-        ok[k] = FULL || v < V;
-        colb[k] = (uint32_t)(v * 16);
+        if constexpr (SPLIT) {
+            ok[k] = FULL || v < VC;
+            colb[k] = (uint32_t)(((int64_t)half * VC + v) * 16);
+        } else {
+            ok[k] = FULL || v < V;
+            colb[k] = (uint32_t)(v * 16);
+        }
     }
 
     const int64_t s0 = R > 0 ? seg_find<VARLEN>(a.seg, r0) : 0;
@@ -93,14 +120,23 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::V
         int nr;
         if (pw.next(a.seg, r1, rs, nr, sg)) {
             const uint32_t bar = bars + 8u * (uint32_t)slot;
-            mbar_arrive_expect_tx(bar, (uint32_t)(2 * nr * row_bytes));
+            if constexpr (SPLIT)
+                mbar_arrive_expect_tx(bar, (uint32_t)nr * 2u * copy_bytes);
+            else
+                mbar_arrive_expect_tx(bar, (uint32_t)(2 * nr * row_bytes));
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
                 if (i >= nr) continue;
                 const uint32_t dst = data + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
-                const int64_t off = (rs + i) * row_bytes;
-                bulk_load(dst, xb + off, (uint32_t)row_bytes, bar);
-                bulk_load(dst + vrow, gb + off, (uint32_t)row_bytes, bar);
+                if constexpr (SPLIT) {
+                    const int64_t off = (rs + i) * row_bytes + copy_off;
+                    bulk_load(dst, xb + off, copy_bytes, bar);
+                    bulk_load(dst + vrow, gb + off, copy_bytes, bar);
+                } else {
+                    const int64_t off = (rs + i) * row_bytes;
+                    bulk_load(dst, xb + off, (uint32_t)row_bytes, bar);
+                    bulk_load(dst + vrow, gb + off, (uint32_t)row_bytes, bar);
+                }
             }
         }
     };
@@ -122,6 +158,7 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::V
     if constexpr (RING) load_stats(r0);
 
     int slot = 0, buf = 0;
+    uint32_t xr = 0;  // split form: row sums exchanged so far
     uint32_t lap = 0;  // completed passes over the ring: the parity of the slot's phase
     bool started = false;  // a previous round exists whose slot can be refilled
     int64_t cur_s = -1;
@@ -304,6 +341,27 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::V
             }
             __syncthreads();
             cta_sum(red[buf], ng, lane, sums);
+            if constexpr (SPLIT) {
+                // Send this half's sums to the other CTA, take its sums, add them in CTA order
+                // (so both CTAs hold the same bits). A round's buffer is written again two
+                // rounds later, after its reader has sent the round in between.
+                const uint32_t par = xr & 1u;
+                if (tid == 0) {
+                    const uint32_t dst = cluster_map(smem_addr(&xch[par][0]), half ^ 1u);
+#pragma unroll
+                    for (int i = 0; i < 2 * RB; ++i) st_cluster_f32(dst + 4u * (uint32_t)i, sums[i]);
+                    mbar_arrive_remote(cluster_map(smem_addr(&xbar[par]), half ^ 1u));
+                }
+                if (!mbar_wait_cluster_bounded(smem_addr(&xbar[par]), (xr >> 1) & 1u, &abort_flag))
+                    err |= kErrTimeout;
+                const volatile float* peer = xch[par];
+#pragma unroll
+                for (int i = 0; i < 2 * RB; ++i) {
+                    const float o = peer[i];
+                    sums[i] = half == 0 ? sums[i] + o : o + sums[i];
+                }
+                ++xr;
+            }
             // dx = rstd * (g - mean(g) - xhat * mean(g*xhat))
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
@@ -348,6 +406,8 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : max_threads(NV, Io<T>::V
         }
     }
     publish_status(err, a.status, a.header);
+    // The split form: neither CTA leaves while the other may still write into its memory.
+    if constexpr (SPLIT) cluster_sync();
 }
 
 // Stage 2: dshift[m] / dscale[m] = sum of the partials of every piece of every segment
@@ -662,9 +722,36 @@ __global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2A
     }
 }
 
-template <typename T, int NV, bool VARLEN, bool RING, bool FULL, bool WIDE = false>
+template <typename T, int NV, bool VARLEN, bool RING, bool FULL, bool WIDE = false, bool SPLIT = false>
 static const void* bwd_fn() {
-    return reinterpret_cast<const void*>(&bwd_kernel<T, NV, VARLEN, RING, FULL, WIDE>);
+    return reinterpret_cast<const void*>(&bwd_kernel<T, NV, VARLEN, RING, FULL, WIDE, SPLIT>);
+}
+
+// The split form: fp32, eight vectors a thread, a ring of half rows.
+static const void* pick_split(bool varlen, bool full) {
+    if (varlen)
+        return full ? bwd_fn<float, 8, true, true, true, false, true>()
+                    : bwd_fn<float, 8, true, true, false, false, true>();
+    return full ? bwd_fn<float, 8, false, true, true, false, true>()
+                : bwd_fn<float, 8, false, true, false, false, true>();
+}
+
+cudaError_t bwd_split_clusters(bool varlen, bool full, int tpb, size_t smem, int* out) {
+    const void* fn = pick_split(varlen, full);
+    cudaError_t e = allow_dynamic_smem(fn);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3((unsigned)tpb);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(out, fn, &cfg);
 }
 
 // Instantiated variants: ring + full row, ring + partial row, plain (partial row).
@@ -710,12 +797,14 @@ cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool fu
 }
 
 cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
-                       int64_t G, int tpb, size_t smem, cudaStream_t stream) {
-    const void* fn = pick_bwd(dtype, nv, varlen, ring, full, tpb);
+                       int64_t G, int tpb, size_t smem, bool split, cudaStream_t stream) {
+    if (split && (dtype != 0 || nv != 8 || !ring || G % 2 != 0 || tpb > kSplitThreads))
+        return cudaErrorInvalidValue;
+    const void* fn = split ? pick_split(varlen, full) : pick_bwd(dtype, nv, varlen, ring, full, tpb);
     if (!fn) return cudaErrorInvalidValue;
     BwdArgs a = args;
     void* params[] = {&a};
-    return launch_dependent(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream);
+    return launch_dependent(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream, split ? 2u : 1u);
 }
 
 cudaError_t launch_stage2(const Stage2Args& args, int dtype, bool varlen, int sms, cudaStream_t stream) {

@@ -23,6 +23,9 @@ __host__ __device__ constexpr int max_threads(int nv, int ve) {
 // Launch bound of the backward's wide form (bf16, four vectors a thread, more threads than
 // max_threads(4, 8)): the row's x and dy are read from the ring twice.
 constexpr int kWideThreads = 512;
+// Launch bound of the backward's split form (fp32 rows too wide for a two-round ring): the
+// two CTAs of a cluster take half a row each, eight vectors a thread.
+constexpr int kSplitThreads = 256;
 
 // A CTA processes its rows in rounds of kRows rows, each thread owning NV 16-byte column
 // vectors of every row. Wider per-thread slices hold fewer rows per round so the values
@@ -321,6 +324,60 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------------------
+// Two-CTA clusters (the backward's split form): the CTAs exchange each row's partial sums
+// through distributed shared memory, announced on an mbarrier of the receiving CTA.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of both CTAs: all shared-memory writes before it are visible to the cluster
+// after it. Used where both CTAs are known to arrive (after set-up, before exit).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior writes.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// mbar_wait_bounded for a barrier another CTA of the cluster arrives on (acquire at cluster
+// scope, so its writes into this CTA's shared memory are visible after it).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (*abort) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // Programmatic dependent launch. Every kernel is launched so that it may be scheduled before
 // the kernel ahead of it in the stream has finished: its CTAs take SMs as that kernel's CTAs
 // retire. Each kernel first lets its own dependents be scheduled, then waits, before any
@@ -334,18 +391,26 @@ __device__ __forceinline__ void pdl_begin() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// cluster: CTAs a cluster along x (1: no clusters).
 inline cudaError_t launch_dependent(const void* fn, dim3 grid, dim3 block, void** params, size_t smem,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, unsigned cluster = 1) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelExC(&cfg, fn, params);
 }
 

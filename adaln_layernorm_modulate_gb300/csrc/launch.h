@@ -22,8 +22,11 @@ cudaError_t launch_stats(const void* x, float* mean, float* rstd, int64_t R, int
 
 cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool full, int tpb,
                               size_t smem, int* out);
+// split: the fp32 split form (G CTAs in clusters of two, G / 2 row tiles).
 cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
-                       int64_t G, int tpb, size_t smem, cudaStream_t stream);
+                       int64_t G, int tpb, size_t smem, bool split, cudaStream_t stream);
+// Resident two-CTA clusters of the split form on the current device.
+cudaError_t bwd_split_clusters(bool varlen, bool full, int tpb, size_t smem, int* out);
 // Stage 2 of a backward on a device of `sms` multiprocessors.
 cudaError_t launch_stage2(const Stage2Args& args, int dtype, bool varlen, int sms, cudaStream_t stream);
 

@@ -85,8 +85,16 @@ SMALL = {
                                              x_mode=synth.ROWS_SCALED, dy_std=0.02),
     # fp32 D=14336: a two-round backward ring of 224 KB, near the per-CTA shared-memory limit.
     "dense-f32-2x19x14336": lambda: synth.dense("c", 124, synth.F32, 2, 19, 14336, dy_std=0.1),
-    # Rows too wide for a two-round backward ring: plain loads, x and dy read twice.
+    # fp32 rows too wide for a two-round backward ring: the split form (two-CTA clusters,
+    # half a row each, row sums exchanged through distributed shared memory); a few rows, many
+    # rows a tile (the exchange buffers cycle), and a packed table of a width the threads do
+    # not cover exactly (D=15360: 240 of 256 lanes) with shared modulation rows.
     "dense-f32-2x21x16384": lambda: synth.dense("c", 119, synth.F32, 2, 21, 16384, dy_std=0.1),
+    "dense-f32-1x1500x16384-split": lambda: synth.dense("c", 127, synth.F32, 1, 1500, 16384,
+                                                        x_mode=synth.ROWS_SCALED, dy_std=0.02),
+    "packed-f32-d15360-split": lambda: synth.make("c", 128, synth.F32, 15360, [700, 3, 0, 250, 47],
+                                                  [1, 0, 2, 1, 1], 3, x_mode=synth.ROWS_SCALED,
+                                                  dy_std=0.02),
     "packed-f32-d128-many": lambda: synth.make(
         "c", 111, synth.F32, 128, list(np.random.default_rng(5).integers(0, 10, 100)),
         list(np.random.default_rng(6).integers(0, 13, 100)), 13),
@@ -219,6 +227,8 @@ def test_shuffled_segment_order_gives_the_same_rows(orc):
 def test_backward_is_bitwise_deterministic():
     for w in (synth.dense("det", 201, synth.BF16, 1, 4000, 1536, x_mode=synth.ROWS_SCALED, dy_std=0.02),
               synth.make("det", 202, synth.BF16, 3072, [300, 5, 2000, 77], [1, 0, 1, 2], 3,
+                         x_mode=synth.ROWS_SCALED, dy_std=0.02),
+              synth.make("det", 203, synth.F32, 16384, [400, 9, 600], [0, 1, 0], 2,
                          x_mode=synth.ROWS_SCALED, dy_std=0.02)):
         d = H.upload(w)
         y, mean, rstd, _ = H.gpu_fwd(d)
@@ -376,7 +386,8 @@ def test_outputs_stay_inside_their_buffers():
 
 @pytest.mark.parametrize("name", ["dense-bf16-2x300x1536", "packed-bf16-d3072-ragged",
                                   "packed-f32-d3072-adversarial", "dense-bf16-d16384",
-                                  "packed-bf16-d8-long-tiles", "packed-bf16-d3072-copy-ring"])
+                                  "packed-bf16-d8-long-tiles", "packed-bf16-d3072-copy-ring",
+                                  "packed-f32-d15360-split"])
 def test_recomputed_statistics_are_bitwise_the_saved_ones(name):
     """A backward that recomputes mean/rstd from x gives bitwise the dx, dshift and dscale of
     the backward that reads the forward's saved statistics."""
