@@ -1,9 +1,10 @@
 """Per-width throughput of the fused forward and backward on the current GPU.
 
     python -m adaln_layernorm_modulate_gb300.widths [--dims 512,1024,...] [--dtype bf16,f32]
+                                                    [--rows N] [--reps N]
 
 For each row width D: one dense batch of random rows (at least 32,760 rows, up to about
-512 MB per tensor), one modulation row; the L2 is flushed by reading a buffer twice its
+512 MB per tensor, or --rows of them), one modulation row; the L2 is flushed by reading a buffer twice its
 size before each timed pair of calls; the median of 20 CUDA-event timings of adaln_fwd and
 of adaln_bwd (partials and reduce). Prints microseconds and the share of the HBM peak
 (algorithmic bytes per call over time; the peak from MEASURED_PEAKS.json when present).
@@ -38,9 +39,9 @@ def peak_gbs() -> float:
         return 6800.0
 
 
-def measure(D: int, dtype: str, dev, flush, fo, reps: int = 20) -> tuple:
+def measure(D: int, dtype: str, dev, flush, fo, reps: int = 20, rows: int = 0) -> tuple:
     code, tdt, e = (ADALN_BF16, torch.bfloat16, 2) if dtype == "bf16" else (ADALN_F32, torch.float32, 4)
-    R = min(262144, max(32760, (512 << 20) // (D * e) // 4 * 4))
+    R = rows if rows > 0 else min(262144, max(32760, (512 << 20) // (D * e) // 4 * 4))
     x = torch.randn(R, D, device=dev).to(tdt)
     dy = (0.02 * torch.randn(R, D, device=dev)).to(tdt)
     shift = (0.1 * torch.randn(1, D, device=dev)).to(tdt)
@@ -83,6 +84,8 @@ def main() -> int:
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--dims", default=DEFAULT_DIMS)
     p.add_argument("--dtype", default="bf16,f32")
+    p.add_argument("--rows", type=int, default=0, help="rows a batch (default: by width, as above)")
+    p.add_argument("--reps", type=int, default=20, help="timed pairs of calls a width")
     args = p.parse_args()
     dev = torch.device("cuda", torch.cuda.current_device())
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (129 << 20)
@@ -92,7 +95,7 @@ def main() -> int:
     print("%-5s %6s %7s | %9s %6s | %9s %6s" % ("dtype", "D", "rows", "fwd us", "peak", "bwd us", "peak"))
     for dtype in args.dtype.split(","):
         for D in (int(v) for v in args.dims.split(",")):
-            R, tf, tb, (bf, bb) = measure(D, dtype, dev, flush, fo)
+            R, tf, tb, (bf, bb) = measure(D, dtype, dev, flush, fo, args.reps, args.rows)
             print("%-5s %6d %7d | %9.1f %5.1f%% | %9.1f %5.1f%%" % (
                 dtype, D, R, tf, 100 * bf / tf / 1e3 / peak, tb, 100 * bb / tb / 1e3 / peak), flush=True)
             torch.cuda.empty_cache()
