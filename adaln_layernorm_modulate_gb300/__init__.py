@@ -19,6 +19,7 @@ from typing import Any
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libadaln.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libadaln_debug.so")  # build(debug=True): index-checked kernels
 
 ADALN_F32, ADALN_BF16 = 0, 1
 STATUS = {
@@ -31,7 +32,7 @@ EXPORTS = (
     "adaln_fwd_varlen_workspace_size", "adaln_fwd_varlen", "adaln_bwd_varlen_workspace_size",
     "adaln_bwd_varlen", "adaln_bwd_varlen_partials", "adaln_bwd_varlen_reduce",
     "adaln_read_status", "adaln_bwd_recompute_workspace_size", "adaln_bwd_recompute",
-    "adaln_bwd_varlen_recompute_workspace_size", "adaln_bwd_varlen_recompute", "adaln_bwd_noalloc", "adaln_noalloc_read_status", "adaln_sum_ranks",
+    "adaln_bwd_varlen_recompute_workspace_size", "adaln_bwd_varlen_recompute", "adaln_bwd_noalloc", "adaln_noalloc_read_status", "adaln_sum_ranks", "adaln_debug_read",
     "adaln_bucket_batch", "adaln_bucket_batch_real",
     "adaln_fit_step_cost", "adaln_bucket_load_cv", "adaln_status_string",
 )
@@ -77,6 +78,7 @@ def _load() -> ctypes.CDLL:
         "adaln_bwd_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp], ci),
         "adaln_noalloc_read_status": ([vp], ci),
         "adaln_sum_ranks": ([vp, vp, i32, i64, vp], ci),
+        "adaln_debug_read": ([vp, ci], ci),
         "adaln_bucket_batch": ([i64, i64, i64, i32], i64),
         "adaln_bucket_batch_real": ([i64, i64, i64, ctypes.c_double], i64),
         "adaln_fit_step_cost": ([vp, vp, vp, i64, ctypes.c_double, ctypes.c_double,
@@ -259,6 +261,18 @@ def adaln_noalloc_read_status(stream=None) -> int:
 def adaln_sum_ranks(parts, out, world, n, stream=None):
     """out[i] = parts[0][i] + ... + parts[world - 1][i], added in rank order (device fp32)."""
     _check("adaln_sum_ranks", lib().adaln_sum_ranks(_ptr(parts), _ptr(out), world, n, _stream(stream)))
+
+
+DEBUG_CLASSES = {1: "rows", 2: "stats", 4: "mod", 8: "partials", 16: "segments", 32: "shared",
+                 64: "grads", 128: "ranks", 256: "status"}  # ADALN_DEBUG_* bits
+
+
+def adaln_debug_read(reset=False) -> int:
+    """The debug build's word of failed index checks since the last reset (0: none); raises
+    AdalnError (ADALN_ERR_UNSUPPORTED) on the release build."""
+    word = ctypes.c_uint32(0)
+    _check("adaln_debug_read", lib().adaln_debug_read(ctypes.addressof(word), 1 if reset else 0))
+    return int(word.value)
 
 
 def adaln_bucket_batch(S, M_mem, M_comp, p) -> int:

@@ -1,5 +1,7 @@
 """Builds libadaln.so in-tree for GB300 (sm_103a): one nvcc per translation unit, in
-parallel, then one link. No CMake, no torch extension machinery."""
+parallel, then one link. No CMake, no torch extension machinery. build(debug=True) makes
+libadaln_debug.so, the same sources compiled with -DADALN_DEBUG (every kernel checks each
+computed index before the access; see adaln_debug_read in include/adaln.h)."""
 from __future__ import annotations
 
 import os
@@ -14,6 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "adaln")
 LIB = os.path.join(PKG, "libadaln.so")
+DEBUG_BUILD = os.path.join(ROOT, "_build", "adaln_debug")
+DEBUG_LIB = os.path.join(PKG, "libadaln_debug.so")
 SOURCES = ["adaln.cu", "fwd.cu", "bwd.cu", "schedule.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -40,22 +44,24 @@ def _inputs() -> list:
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not verbose_ptxas and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    lib_path, objdir = (DEBUG_LIB, DEBUG_BUILD) if debug else (LIB, BUILD)
+    if not force and not verbose_ptxas and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
+    extra = ["-DADALN_DEBUG"] if debug else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc] + flags(verbose_ptxas) + ["-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
+        cmd = [cc] + flags(verbose_ptxas) + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed for %s:\n%s%s" % (src, r.stdout, r.stderr))
@@ -66,12 +72,11 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if verbose_ptxas:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib_path + ".tmp%d" % os.getpid()
     subprocess.check_call([cc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(force=True, verbose_ptxas="-v" in sys.argv)
-    print(LIB)
+    print(build(force=True, verbose_ptxas="-v" in sys.argv, debug="--debug" in sys.argv))

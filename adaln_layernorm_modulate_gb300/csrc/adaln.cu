@@ -811,3 +811,19 @@ extern "C" int adaln_sum_ranks(const float* parts, float* out, int32_t world, in
     if (sms <= 0) return ADALN_ERR_CUDA;
     return launched(launch_rank_sum(parts, out, world, n, sms, stream));
 }
+
+extern "C" int adaln_debug_read(uint32_t* word, int reset) {
+#ifdef ADALN_DEBUG
+    if (word == nullptr) return ADALN_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ADALN_ERR_CUDA;
+    uint32_t f = 0, b = 0;
+    if (debug_word_fwd(&f, reset != 0) != cudaSuccess || debug_word_bwd(&b, reset != 0) != cudaSuccess)
+        return ADALN_ERR_CUDA;
+    *word = f | b;
+    return ADALN_OK;
+#else
+    (void)word;
+    (void)reset;
+    return ADALN_ERR_UNSUPPORTED;
+#endif
+}

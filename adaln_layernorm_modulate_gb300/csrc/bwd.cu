@@ -130,12 +130,18 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
                 const uint32_t dst = data + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
                 if constexpr (SPLIT) {
                     const int64_t off = (rs + i) * row_bytes + copy_off;
-                    bulk_load(dst, xb + off, copy_bytes, bar);
-                    bulk_load(dst + vrow, gb + off, copy_bytes, bar);
+                    if (ADALN_IN_ROW(rs + i, R, copy_off, copy_bytes, row_bytes) &&
+                        ADALN_IN_RING(bars, dst, copy_bytes) && ADALN_IN_RING(bars, dst + vrow, copy_bytes)) {
+                        bulk_load(dst, xb + off, copy_bytes, bar);
+                        bulk_load(dst + vrow, gb + off, copy_bytes, bar);
+                    }
                 } else {
                     const int64_t off = (rs + i) * row_bytes;
-                    bulk_load(dst, xb + off, (uint32_t)row_bytes, bar);
-                    bulk_load(dst + vrow, gb + off, (uint32_t)row_bytes, bar);
+                    if (ADALN_IN_ROW(rs + i, R, 0, row_bytes, row_bytes) && ADALN_IN_RING(bars, dst, row_bytes) &&
+                        ADALN_IN_RING(bars, dst + vrow, row_bytes)) {
+                        bulk_load(dst, xb + off, (uint32_t)row_bytes, bar);
+                        bulk_load(dst + vrow, gb + off, (uint32_t)row_bytes, bar);
+                    }
                 }
             }
         }
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
     auto load_stats = [&](int64_t first) {
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
-            const bool in = first + i < r1;
+            const bool in = first + i < r1 && ADALN_IN(kDbgStats, first + i >= 0 && first + i < R);
             mu_n[i] = in ? __ldg(a.mean + first + i) : 0.0f;
             rs_n[i] = in ? __ldg(a.rstd + first + i) : 0.0f;
         }
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
         const int64_t slot = b + cur_s;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            if (ok[k]) {
+            if (ok[k] && ADALN_IN(kDbgPartials, slot >= 0 && slot < S && (int64_t)colb[k] / 16 < V)) {
                 const int64_t v = colb[k] / 16;  // my vector k
                 float* p0 = a.vec_major ? a.partials + ((v * 2 + 0) * S + slot) * VE
                                         : a.partials + slot * 2 * D + v * VE;
@@ -218,7 +224,8 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
                     const uint32_t xs = my_vec + (uint32_t)slot * vslot + (uint32_t)(2 * i) * vrow;
 #pragma unroll
                     for (int k = 0; k < NV; ++k) {
-                        const bool on = i < nr && ok[k];
+                        const bool on = i < nr && ok[k] && ADALN_IN_RING(bars, xs + (uint32_t)k * vk, 16) &&
+                                        ADALN_IN_RING(bars, xs + vrow + (uint32_t)k * vk, 16);
                         xv[i][k] = on ? lds128(xs + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
                         gv[i][k] = on ? lds128(xs + vrow + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
                     }
@@ -230,12 +237,13 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
                 const int64_t off = (row + i) * row_bytes;
 #pragma unroll
                 for (int k = 0; k < NV; ++k) {
-                    const bool on = i < nr && ok[k];
+                    const bool on = i < nr && ok[k] && ADALN_IN_ROW(row + i, R, colb[k], 16, row_bytes);
                     xv[i][k] = on ? ld_stream(xb + off + colb[k]) : make_uint4(0, 0, 0, 0);
                     gv[i][k] = on ? ld_stream(gb + off + colb[k]) : make_uint4(0, 0, 0, 0);
                 }
-                mu[i] = i < nr ? __ldg(a.mean + row + i) : 0.0f;
-                rs[i] = i < nr ? __ldg(a.rstd + row + i) : 0.0f;
+                const bool in = i < nr && ADALN_IN(kDbgStats, row + i >= 0 && row + i < R);
+                mu[i] = in ? __ldg(a.mean + row + i) : 0.0f;
+                rs[i] = in ? __ldg(a.rstd + row + i) : 0.0f;
             }
         }
 
@@ -248,7 +256,8 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
                 uint4 vc = make_uint4(0, 0, 0, 0);
-                if (cur_ok && ok[k]) vc = ld_keep(static_cast<const char*>(a.scale) + m * row_bytes + colb[k]);
+                if (cur_ok && ok[k] && ADALN_IN(kDbgMod, m >= 0 && m < a.seg.nmod && colb[k] + 16 <= row_bytes))
+                    vc = ld_keep(static_cast<const char*>(a.scale) + m * row_bytes + colb[k]);
                 IO::unpackp(vc, sc1[k]);
                 const f2r one = p_splat(1.0f);
 #pragma unroll
@@ -265,8 +274,10 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
             f2r sg[2] = {kPairZero, kPairZero}, sgx[2] = {kPairZero, kPairZero};
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
-                const uint4 xq = ok[k] ? lds128(xs + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
-                const uint4 gq = ok[k] ? lds128(xs + vrow + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                const bool on = ok[k] && ADALN_IN_RING(bars, xs + (uint32_t)k * vk, 16) &&
+                                ADALN_IN_RING(bars, xs + vrow + (uint32_t)k * vk, 16);
+                const uint4 xq = on ? lds128(xs + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
+                const uint4 gq = on ? lds128(xs + vrow + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
                 f2r xh[PV], fd[PV];
                 IO::unpackp(xq, xh);
                 IO::unpackp(gq, fd);
@@ -293,7 +304,9 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
             char* dxr = dxb + row * row_bytes;
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
-                if (!ok[k]) continue;
+                if (!ok[k] || !ADALN_IN_RING(bars, xs + (uint32_t)k * vk, 16) ||
+                    !ADALN_IN_RING(bars, xs + vrow + (uint32_t)k * vk, 16))
+                    continue;
                 f2r xh[PV], fd[PV], o[PV];
                 IO::unpackp(lds128(xs + (uint32_t)k * vk), xh);
                 IO::unpackp(lds128(xs + vrow + (uint32_t)k * vk), fd);
@@ -302,7 +315,7 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
                     xh[p] = p_mul(p_sub(xh[p], mu2), rs2);
                     o[p] = p_fma(p_fma(xh[p], nmgx, p_mul(fd[p], sc1[k][p])), rs2, nmgr);
                 }
-                st_vec(dxr + colb[k], IO::packp(o));
+                if (ADALN_IN_ROW(row, R, colb[k], 16, row_bytes)) st_vec(dxr + colb[k], IO::packp(o));
             }
             buf ^= 1;
         } else if (cur_ok) {  // uniform across the CTA
@@ -375,7 +388,7 @@ __global__ void __launch_bounds__(SPLIT ? kSplitThreads : WIDE ? kWideThreads : 
                     f2r o[PV];
 #pragma unroll
                     for (int p = 0; p < PV; ++p) o[p] = p_fma(p_fma(xh[i][k][p], nmgx, g[i][k][p]), rs2, nmgr);
-                    st_vec(dxr + colb[k], IO::packp(o));
+                    if (ADALN_IN_ROW(row + i, R, colb[k], 16, row_bytes)) st_vec(dxr + colb[k], IO::packp(o));
                 }
             }
             buf ^= 1;
@@ -442,7 +455,7 @@ __device__ __forceinline__ void compact_hits(const Segments& sg, int64_t m, int6
         const int64_t s = s0 + i;
         np[i] = 0;
         sl[i] = 0;
-        if (s < sg.nseg && (int64_t)__ldg(sg.mod + s) == m) {
+        if (s < sg.nseg && ADALN_IN(kDbgSegments, s >= 0) && (int64_t)__ldg(sg.mod + s) == m) {
             // Clamp into [0, R] so a malformed table cannot index past the slots.
             const int64_t lo = max((int64_t)0, min(seg_start<true>(sg, s), R));
             const int64_t hi = max((int64_t)0, min(seg_start<true>(sg, s + 1), R));
@@ -486,14 +499,14 @@ __device__ __forceinline__ void compact_hits(const Segments& sg, int64_t m, int6
     }
 #pragma unroll
     for (int i = 0; i < kStage2Per; ++i) {
-        if (np[i] > 0) {
+        if (np[i] > 0 && ADALN_IN(kDbgShared, oh >= 0 && oh < kStage2Chunk)) {
             hit_slot[oh] = sl[i];
             hit_first[oh] = op;
             ++oh;
             op += np[i];
         }
     }
-    if (tid == 0) hit_first[H] = NP;
+    if (tid == 0 && ADALN_IN(kDbgShared, H >= 0 && H <= kStage2Chunk)) hit_first[H] = NP;
     __syncthreads();
 }
 
@@ -553,10 +566,15 @@ __global__ void __launch_bounds__(kStage2Threads) stage2v_kernel(const Stage2Arg
                         const int64_t q = q0 + (int64_t)i * splits;
                         if (q < n) {
                             const int64_t slot = slot_of(q);
+                            if (ADALN_IN(kDbgPartials, slot >= 0 && slot < S)) {
 #pragma unroll
-                            for (int j = 0; j < Q; ++j) {
-                                u[i][j] = __ldg(P0 + slot * Q + j);
-                                w[i][j] = __ldg(P1 + slot * Q + j);
+                                for (int j = 0; j < Q; ++j) {
+                                    u[i][j] = __ldg(P0 + slot * Q + j);
+                                    w[i][j] = __ldg(P1 + slot * Q + j);
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < Q; ++j) u[i][j] = w[i][j] = make_float4(0.f, 0.f, 0.f, 0.f);
                             }
                         }
                     }
@@ -598,7 +616,7 @@ __global__ void __launch_bounds__(kStage2Threads) stage2v_kernel(const Stage2Arg
 #pragma unroll
                 for (int e = 0; e < 2 * VE; ++e) acc[e] += __shfl_xor_sync(0xFFFFFFFFu, acc[e], o);
             }
-            if (k == 0 && vok) {
+            if (k == 0 && vok && ADALN_IN(kDbgGrads, m >= 0 && m < a.seg.nmod && v >= 0 && v < V)) {
                 float4* o0 = reinterpret_cast<float4*>(a.dshift + m * a.D + v * VE);
                 float4* o1 = reinterpret_cast<float4*>(a.dscale + m * a.D + v * VE);
 #pragma unroll
@@ -625,7 +643,8 @@ __global__ void __launch_bounds__(kStage2Threads) stage2v_kernel(const Stage2Arg
             if (tid < nvb * 2 * VE) {
                 const int vv = tid / (2 * VE), e = tid % (2 * VE);
                 const int64_t vg = (int64_t)blockIdx.x * nvb + vv;
-                if (vg < V) {
+                if (vg < V && ADALN_IN(kDbgGrads, m >= 0 && m < a.seg.nmod && vg >= 0) &&
+                    ADALN_IN(kDbgShared, vv * wpv + wpv <= NW)) {
                     float t = red[vv * wpv][e];
                     for (int w2 = 1; w2 < wpv; ++w2) t += red[vv * wpv + w2][e];
                     float* out = e < VE ? a.dshift : a.dscale;
@@ -670,8 +689,12 @@ __global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2A
                         const int64_t q = q0 + (int64_t)i * splits;
                         if (q < n) {
                             const int64_t slot = slot_of(q);
-                            u[i] = __ldg(P + (slot * 2 + 0) * D4);
-                            v[i] = __ldg(P + (slot * 2 + 1) * D4);
+                            if (ADALN_IN(kDbgPartials, slot >= 0 && slot < a.S)) {
+                                u[i] = __ldg(P + (slot * 2 + 0) * D4);
+                                v[i] = __ldg(P + (slot * 2 + 1) * D4);
+                            } else {
+                                u[i] = v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
                         }
                     }
 #pragma unroll
@@ -714,7 +737,7 @@ __global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2A
             }
             __syncthreads();
         }
-        if (k == 0 && cok) {
+        if (k == 0 && cok && ADALN_IN(kDbgGrads, m >= 0 && m < a.seg.nmod && c4 >= 0)) {
             reinterpret_cast<float4*>(a.dshift)[m * D4 + c4] = red[0][tid];
             reinterpret_cast<float4*>(a.dscale)[m * D4 + c4] = red[1][tid];
         }
@@ -807,6 +830,8 @@ cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool
     return launch_dependent(fn, dim3((unsigned)G), dim3((unsigned)tpb), params, smem, stream, split ? 2u : 1u);
 }
 
+cudaError_t debug_word_bwd(uint32_t* out, bool reset) { return debug_word(out, reset); }
+
 cudaError_t launch_stage2(const Stage2Args& args, int dtype, bool varlen, int sms, cudaStream_t stream) {
     dim3 grid;
     const void* fn;
@@ -855,6 +880,7 @@ __global__ void __launch_bounds__(256) rank_sum_kernel(const float* __restrict__
         const float4* p4 = reinterpret_cast<const float4*>(parts);
         float4* o4 = reinterpret_cast<float4*>(out);
         for (int64_t i = first; i < n4; i += stride) {
+            if (!ADALN_IN(kDbgRanks, i >= 0 && world >= 1)) continue;
             float4 s = __ldg(p4 + i);
             for (int32_t r = 1; r < world; ++r) {
                 const float4 v = __ldg(p4 + (int64_t)r * n4 + i);
@@ -864,6 +890,7 @@ __global__ void __launch_bounds__(256) rank_sum_kernel(const float* __restrict__
         }
     } else {
         for (int64_t i = first; i < n; i += stride) {
+            if (!ADALN_IN(kDbgRanks, i >= 0 && world >= 1)) continue;
             float s = __ldg(parts + i);
             for (int32_t r = 1; r < world; ++r) s += __ldg(parts + (int64_t)r * n + i);
             out[i] = s;

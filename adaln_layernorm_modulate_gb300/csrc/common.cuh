@@ -39,6 +39,58 @@ struct RowShape {
 
 };
 
+// ---------------------------------------------------------------------------------------
+// Debug builds (-DADALN_DEBUG, libadaln_debug.so): each computed index of a global or
+// shared-memory access is checked against the extent of its buffer first. A failed check
+// skips the access (a load yields zeros) and sets its class bit in the module's debug word,
+// which adaln_debug_read returns; nothing traps. Release builds compile the checks away
+// (ADALN_IN is the constant true and evaluates nothing).
+// ---------------------------------------------------------------------------------------
+enum : uint32_t {
+    kDbgRows = 1u,       // x, dy, y, dx: row in [0, R), bytes within the row
+    kDbgStats = 2u,      // mean, rstd: row in [0, R)
+    kDbgMod = 4u,        // shift, scale: modulation row in [0, nmod), bytes within the row
+    kDbgPartials = 8u,   // backward partials: slot in [0, S), column in [0, D)
+    kDbgSegments = 16u,  // cu_seqlens[0 .. nseg], mod_idx[0 .. nseg)
+    kDbgShared = 32u,    // shared-memory ring: within the launch's dynamic shared memory
+    kDbgGrads = 64u,     // dshift, dscale: [0, nmod) x [0, D)
+    kDbgRanks = 128u,    // rank sum: [0, n) of each rank's array and of the output
+    kDbgStatus = 256u,   // status words: [0, kMaxCtas)
+};
+#ifdef ADALN_DEBUG
+static __device__ unsigned int g_adaln_debug;  // one per translation unit (module)
+static __device__ __noinline__ void debug_fail(uint32_t cls) { atomicOr(&g_adaln_debug, cls); }
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+#define ADALN_IN(cls, cond) ((cond) || (::adaln::debug_fail(cls), false))
+// [addr, addr + bytes) within the dynamic shared memory that starts at shared address base.
+#define ADALN_IN_RING(base, addr, bytes) \
+    ADALN_IN(::adaln::kDbgShared,        \
+             (addr) >= (base) && (uint64_t)((addr) - (base)) + (uint64_t)(bytes) <= ::adaln::dynamic_smem_bytes())
+// The module's debug word, optionally cleared (host side).
+static inline cudaError_t debug_word(uint32_t* out, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_adaln_debug, sizeof(uint32_t));
+    if (e == cudaSuccess && reset) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_adaln_debug, &zero, sizeof(uint32_t));
+    }
+    return e;
+}
+#else
+#define ADALN_IN(cls, cond) true
+#define ADALN_IN_RING(base, addr, bytes) true
+static inline cudaError_t debug_word(uint32_t* out, bool) {
+    *out = 0;
+    return cudaSuccess;
+}
+#endif
+// Row r of a tensor of R rows, bytes [off, off + n) of a row of rb bytes.
+#define ADALN_IN_ROW(r, R, off, n, rb) \
+    ADALN_IN(::adaln::kDbgRows, (r) >= 0 && (r) < (R) && (int64_t)(off) + (int64_t)(n) <= (int64_t)(rb))
+
 // Workspace layout: [header | one status word per CTA | backward partials].
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kStatusWordsBytes = sizeof(uint32_t) * kMaxCtas;
@@ -127,13 +179,13 @@ __device__ __forceinline__ int64_t tile_of_row(int64_t r, int64_t R, int64_t G) 
 
 template <bool VARLEN>
 __device__ __forceinline__ int64_t seg_start(const Segments& sg, int64_t s) {
-    if constexpr (VARLEN) return (int64_t)__ldg(sg.cu + s);
+    if constexpr (VARLEN) return ADALN_IN(kDbgSegments, s >= 0 && s <= sg.nseg) ? (int64_t)__ldg(sg.cu + s) : 0;
     else return s * sg.N;
 }
 
 template <bool VARLEN>
 __device__ __forceinline__ int64_t seg_mod(const Segments& sg, int64_t s) {
-    if constexpr (VARLEN) return (int64_t)__ldg(sg.mod + s);
+    if constexpr (VARLEN) return ADALN_IN(kDbgSegments, s >= 0 && s < sg.nseg) ? (int64_t)__ldg(sg.mod + s) : -1;
     else return s;
 }
 
@@ -163,12 +215,13 @@ __device__ uint32_t validate_segments(const Segments& sg, int64_t b, int64_t G) 
         uint32_t e = 0;
         const int64_t s0 = b * sg.nseg / G, s1 = (b + 1) * sg.nseg / G;
         for (int64_t s = s0 + threadIdx.x; s < s1; s += blockDim.x) {
+            if (!ADALN_IN(kDbgSegments, s >= 0 && s < sg.nseg)) continue;
             const int64_t a = __ldg(sg.cu + s), c = __ldg(sg.cu + s + 1);
             if (a > c || a < 0 || c > sg.R) e |= kErrSeqlens;
             const int64_t m = __ldg(sg.mod + s);
             if (m < 0 || m >= sg.nmod) e |= kErrModIdx;
         }
-        if (b == 0 && threadIdx.x == 0) {
+        if (b == 0 && threadIdx.x == 0 && ADALN_IN(kDbgSegments, sg.nseg >= 0)) {
             if (__ldg(sg.cu) != 0 || (int64_t)__ldg(sg.cu + sg.nseg) != sg.R) e |= kErrSeqlens;
         }
         return e;
@@ -182,7 +235,7 @@ __device__ __forceinline__ void publish_status(uint32_t err, uint32_t* words, Ws
     if (__syncthreads_or((int)(err & kErrSeqlens))) all |= kErrSeqlens;
     if (__syncthreads_or((int)(err & kErrModIdx))) all |= kErrModIdx;
     if (__syncthreads_or((int)(err & kErrTimeout))) all |= kErrTimeout;
-    if (words == nullptr || threadIdx.x != 0) return;
+    if (words == nullptr || threadIdx.x != 0 || !ADALN_IN(kDbgStatus, blockIdx.x < kMaxCtas)) return;
     words[blockIdx.x] = all;
     if (blockIdx.x == 0) {
         header->magic = kStatusMagic;

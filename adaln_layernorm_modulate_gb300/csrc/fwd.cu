@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const F
             mbar_arrive_expect_tx(bar, (uint32_t)(nr * row_bytes));
 #pragma unroll
             for (int i = 0; i < RB; ++i)
-                if (i < nr)
+                if (i < nr && ADALN_IN_ROW(rs + i, R, 0, row_bytes, row_bytes) &&
+                    ADALN_IN_RING(bars, data + (uint32_t)slot * vslot + (uint32_t)i * vrow, row_bytes))
                     bulk_load(data + (uint32_t)slot * vslot + (uint32_t)i * vrow, xb + (rs + i) * row_bytes,
                               (uint32_t)row_bytes, bar);
         }
@@ -117,13 +118,16 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const F
         if (pw.next(a.seg, r1, rs, nr, sg)) {
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                if (i >= nr) continue;
+                if (i >= nr || !ADALN_IN_ROW(rs + i, R, 0, 4, row_bytes)) continue;
                 const char* src = xb + (rs + i) * row_bytes;
                 const uint32_t dst = my_vec + (uint32_t)slot * vslot + (uint32_t)i * vrow;
-                cp_async4_sa(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow, src);
+                if (ADALN_IN_RING(bars, my_k + (uint32_t)slot * kslot + (uint32_t)i * krow, 4))
+                    cp_async4_sa(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow, src);
 #pragma unroll
                 for (int k = 0; k < NV; ++k)
-                    if (ok[k]) cp_async16_sa(dst + (uint32_t)k * vk, src + colb[k]);
+                    if (ok[k] && ADALN_IN_ROW(rs + i, R, colb[k], 16, row_bytes) &&
+                        ADALN_IN_RING(bars, dst + (uint32_t)k * vk, 16))
+                        cp_async16_sa(dst + (uint32_t)k * vk, src + colb[k]);
             }
         }
         cp_async_commit();
@@ -158,8 +162,11 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const F
                 const uint32_t rowsa = (uint32_t)slot * vslot + (uint32_t)i * vrow;
 #pragma unroll
                 for (int k = 0; k < NV; ++k)
-                    xv[i][k] = (i < nr && ok[k]) ? lds128(my_vec + rowsa + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
-                K[i] = (i < nr) ? IO::first_of_word(lds32(data + rowsa)) : 0.0f;
+                    xv[i][k] = (i < nr && ok[k] && ADALN_IN_RING(bars, my_vec + rowsa + (uint32_t)k * vk, 16))
+                                   ? lds128(my_vec + rowsa + (uint32_t)k * vk)
+                                   : make_uint4(0, 0, 0, 0);
+                K[i] = (i < nr && ADALN_IN_RING(bars, data + rowsa, 4)) ? IO::first_of_word(lds32(data + rowsa))
+                                                                          : 0.0f;
             }
         } else if constexpr (COPY) {
             cp_async_wait(ns - 1);  // this thread's copies of this round have landed
@@ -168,9 +175,12 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const F
                 const uint32_t src = my_vec + (uint32_t)slot * vslot + (uint32_t)i * vrow;
 #pragma unroll
                 for (int k = 0; k < NV; ++k)
-                    xv[i][k] = (i < nr && ok[k]) ? lds128(src + (uint32_t)k * vk) : make_uint4(0, 0, 0, 0);
-                K[i] = (i < nr) ? IO::first_of_word(lds32(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow))
-                                : 0.0f;
+                    xv[i][k] = (i < nr && ok[k] && ADALN_IN_RING(bars, src + (uint32_t)k * vk, 16))
+                                   ? lds128(src + (uint32_t)k * vk)
+                                   : make_uint4(0, 0, 0, 0);
+                K[i] = (i < nr && ADALN_IN_RING(bars, my_k + (uint32_t)slot * kslot + (uint32_t)i * krow, 4))
+                           ? IO::first_of_word(lds32(my_k + (uint32_t)slot * kslot + (uint32_t)i * krow))
+                           : 0.0f;
             }
         } else {
 #pragma unroll
@@ -178,8 +188,10 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const F
                 const char* src = xb + (row + i) * row_bytes;
 #pragma unroll
                 for (int k = 0; k < NV; ++k)
-                    xv[i][k] = (i < nr && ok[k]) ? ld_stream(src + colb[k]) : make_uint4(0, 0, 0, 0);
-                K[i] = (i < nr) ? IO::first(src) : 0.0f;
+                    xv[i][k] = (i < nr && ok[k] && ADALN_IN_ROW(row + i, R, colb[k], 16, row_bytes))
+                                   ? ld_stream(src + colb[k])
+                                   : make_uint4(0, 0, 0, 0);
+                K[i] = (i < nr && ADALN_IN_ROW(row + i, R, 0, 4, row_bytes)) ? IO::first(src) : 0.0f;
             }
         }
 
@@ -192,7 +204,7 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const F
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
                 uint4 vs = make_uint4(0, 0, 0, 0), vc = make_uint4(0, 0, 0, 0);
-                if (cur_ok && ok[k]) {
+                if (cur_ok && ok[k] && ADALN_IN(kDbgMod, m >= 0 && m < a.seg.nmod && colb[k] + 16 <= row_bytes)) {
                     vs = ld_keep(static_cast<const char*>(a.shift) + m * row_bytes + colb[k]);
                     vc = ld_keep(static_cast<const char*>(a.scale) + m * row_bytes + colb[k]);
                 }
@@ -272,9 +284,9 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) fwd_kernel(const F
                     f2r o[PV];
 #pragma unroll
                     for (int p = 0; p < PV; ++p) o[p] = p_fma(p_mul(d[i][k][p], prs), sc1[k][p], sh[k][p]);
-                    st_vec(yr + colb[k], IO::packp(o));
+                    if (ADALN_IN_ROW(row + i, R, colb[k], 16, row_bytes)) st_vec(yr + colb[k], IO::packp(o));
                 }
-                if (tid == 0) {
+                if (tid == 0 && ADALN_IN(kDbgStats, row + i >= 0 && row + i < R)) {
                     a.mean[row + i] = K[i] + md[i];
                     a.rstd[row + i] = rs;
                 }
@@ -415,12 +427,15 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) stats_kernel(const
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
             const char* src = xb + (row + i) * row_bytes;
-            K[i] = i < nr ? IO::first(src) : 0.0f;
+            K[i] = (i < nr && ADALN_IN_ROW(row + i, R, 0, 4, row_bytes)) ? IO::first(src) : 0.0f;
             const f2r kk = p_splat(K[i]);
             f2r acc0 = kPairZero, acc1 = kPairZero;
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
-                IO::unpackp((i < nr && ok[k]) ? ld_stream(src + colb[k]) : make_uint4(0, 0, 0, 0), d[i][k]);
+                IO::unpackp((i < nr && ok[k] && ADALN_IN_ROW(row + i, R, colb[k], 16, row_bytes))
+                                ? ld_stream(src + colb[k])
+                                : make_uint4(0, 0, 0, 0),
+                            d[i][k]);
 #pragma unroll
                 for (int p = 0; p < PV; ++p) {
                     d[i][k][p] = p_sub(d[i][k][p], kk);
@@ -466,7 +481,7 @@ __global__ void __launch_bounds__(max_threads(NV, Io<T>::VE)) stats_kernel(const
         if (tid == 0) {
 #pragma unroll
             for (int i = 0; i < RB; ++i) {
-                if (i < nr) {
+                if (i < nr && ADALN_IN(kDbgStats, row + i >= 0 && row + i < R)) {
                     mean[row + i] = K[i] + md[i];
                     rstd[row + i] = rsqrtf(s2[i] * invD + eps);
                 }
@@ -487,6 +502,8 @@ static const void* pick_stats(int nv) {
         default: return nullptr;
     }
 }
+
+cudaError_t debug_word_fwd(uint32_t* out, bool reset) { return debug_word(out, reset); }
 
 cudaError_t launch_stats(const void* x, float* mean, float* rstd, int64_t R, int64_t D, float eps,
                          int dtype, int nv, int tpb, int64_t G, cudaStream_t stream) {

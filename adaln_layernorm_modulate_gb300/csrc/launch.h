@@ -25,6 +25,10 @@ cudaError_t bwd_blocks_per_sm(int dtype, int nv, bool varlen, bool ring, bool fu
 // split: the fp32 split form (G CTAs in clusters of two, G / 2 row tiles).
 cudaError_t launch_bwd(const BwdArgs& args, int dtype, int nv, bool varlen, bool ring, bool full,
                        int64_t G, int tpb, size_t smem, bool split, cudaStream_t stream);
+// Debug builds: the debug word of the forward's and the backward's module (0 in release
+// builds), cleared after the read when `reset`.
+cudaError_t debug_word_fwd(uint32_t* out, bool reset);
+cudaError_t debug_word_bwd(uint32_t* out, bool reset);
 // Resident two-CTA clusters of the split form on the current device.
 cudaError_t bwd_split_clusters(bool varlen, bool full, int tpb, size_t smem, int* out);
 // Stage 2 of a backward on a device of `sms` multiprocessors.

@@ -237,6 +237,27 @@ int adaln_noalloc_read_status(cudaStream_t stream);
  * `stream`. Returns ADALN_ERR_INVALID_ARG for world < 1 or n < 0. */
 int adaln_sum_ranks(const float* parts, float* out, int32_t world, int64_t n, cudaStream_t stream);
 
+/* ---- Debug build --------------------------------------------------------------------------
+ * The library can be built a second time with -DADALN_DEBUG (libadaln_debug.so; the package's
+ * build(debug=True)). In that build every kernel checks each computed index of a global or
+ * shared-memory access against the extent of its buffer before the access; a failed check
+ * skips the access (a load yields zeros) and sets the access's class bit in a device-side
+ * debug word, without trapping. adaln_debug_read waits for the device (cudaDeviceSynchronize)
+ * and stores in *word the OR of the bits set since the last reset (0: no check failed); with
+ * reset != 0 it also clears them. Returns ADALN_ERR_INVALID_ARG for a null word, ADALN_ERR_CUDA
+ * if the device reports an error, and ADALN_ERR_UNSUPPORTED from the release build, which
+ * compiles the checks away. */
+#define ADALN_DEBUG_ROWS     1u   /* x, dy, y, dx: row in [0, R), bytes within the row        */
+#define ADALN_DEBUG_STATS    2u   /* mean, rstd: row in [0, R)                                */
+#define ADALN_DEBUG_MOD      4u   /* shift, scale: modulation row in [0, nmod)                */
+#define ADALN_DEBUG_PARTIALS 8u   /* backward partials: slot in [0, tiles + nseg), column < D */
+#define ADALN_DEBUG_SEGMENTS 16u  /* cu_seqlens[0 .. nseg], mod_idx[0 .. nseg)                */
+#define ADALN_DEBUG_SHARED   32u  /* shared memory: within the CTA's allocation               */
+#define ADALN_DEBUG_GRADS    64u  /* dshift, dscale: [0, nmod) x [0, D)                       */
+#define ADALN_DEBUG_RANKS    128u /* adaln_sum_ranks: [0, n) of each rank's row              */
+#define ADALN_DEBUG_STATUS   256u /* workspace status words                                   */
+int adaln_debug_read(uint32_t* word, int reset);
+
 /* Dual-constraint bucket size, AdaptiveLoad technical summary section 2.A:
  *     B = max(1, min(floor(M_mem / S), floor(M_comp / S^p)))
  * with exact integer arithmetic (S^p is never formed past M_comp). Host only.

@@ -37,6 +37,27 @@ def test_library_exports_every_declared_symbol():
         assert getattr(lib, name) is not None
 
 
+def test_debug_library_exports_every_declared_symbol():
+    if not os.path.exists(A.DEBUG_LIB_PATH):
+        pytest.skip("libadaln_debug.so not built")
+    out = subprocess.run(["nm", "-D", "--defined-only", A.DEBUG_LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (adaln_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+
+
+def test_release_library_has_no_debug_word():
+    # The release build compiles the index checks away: adaln_debug_read answers
+    # ADALN_ERR_UNSUPPORTED before any device work (and rejects nothing else first).
+    word = ctypes.c_uint32(7)
+    assert A.lib().adaln_debug_read(ctypes.addressof(word), 0) == 2
+    assert A.lib().adaln_debug_read(None, 1) == 2
+    assert word.value == 7
+    with pytest.raises(A.AdalnError):
+        A.adaln_debug_read()
+
+
 def test_bucket_batch_matches_oracle_and_brute_force():
     for S, M_mem, M_comp, p in itertools.product(range(1, 24), (1, 5, 17, 64, 100),
                                                  (1, 9, 50, 333, 1000), (1, 2, 3)):
