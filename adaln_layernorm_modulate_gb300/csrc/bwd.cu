@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2A
         red[1][tid] = acc1;
         __syncthreads();
         for (int st = splits / 2; st >= 1; st >>= 1) {
-            if (k < st) {
+            if (k < st && ADALN_IN(kDbgShared, tid + st * cw < kStage2Threads)) {
                 const float4 u = red[0][tid + st * cw], v = red[1][tid + st * cw];
                 float4& p = red[0][tid];
                 float4& q = red[1][tid];
