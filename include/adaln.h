@@ -96,7 +96,9 @@ size_t adaln_bwd_workspace_size(int64_t Bt, int64_t N, int64_t D, adaln_dtype dt
  * and dshift/dscale [Bt, D] (fp32, overwritten). Section 2.B, backward-pass bullet ("D-tile
  * coalesced reduction"): each row's dx is computed from the saved statistics while threads
  * pinned to feature indices accumulate dy and dy*xhat down their tile of rows; per-tile
- * partials are summed by a second, fixed-order stage. Two launches on `stream`. */
+ * partials are summed by a second, fixed-order stage. Two launches on `stream`; for fp32
+ * rows wider than 14456 the first is a launch of two-CTA thread-block clusters (each CTA
+ * half of every row), so such calls need a device and context that allow clusters. */
 int adaln_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
               const void* scale, void* dx, float* dshift, float* dscale, void* workspace,
               size_t workspace_bytes, int64_t Bt, int64_t N, int64_t D, adaln_dtype dtype,
