@@ -78,8 +78,8 @@ typedef enum {
     ADALN_ERR_BAD_MOD_IDX = 7,  /* device data: mod_idx out of range (adaln_read_status) */
     ADALN_ERR_TIMEOUT = 8       /* a kernel gave up waiting (1 s) for a bulk copy of its
                                    input rows, or for the row sums of the other CTA of its
-                                   cluster (fp32 rows wider than 14456); the rows it had not
-                                   finished are unwritten (adaln_read_status) */
+                                   cluster (fp32 rows wider than 14456); its outputs from
+                                   then on are not valid (adaln_read_status) */
 } adaln_status;
 
 /* Forward, dense batch x[Bt, N, D]; token (b, n) uses shift[b], scale[b].
