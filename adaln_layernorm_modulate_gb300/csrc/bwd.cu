@@ -24,7 +24,7 @@ namespace adaln {
 // WIDE: bf16 rows of four vectors a thread over more than max_threads(4, 8) threads (D of
 // 14336 and 16384: 448 and 512 threads), which read x and dy from the ring twice so that only
 // the column accumulators and (1 + scale) stay in registers (128 a thread at 512).
-// SPLIT: fp32 rows too wide for a ring of two rounds (D > 14456). The grid is made of
+// SPLIT: fp32 rows too wide for a ring of two rounds (D > 14336). The grid is made of
 // two-CTA clusters, a cluster per row tile; CTA r of a cluster stages and owns half r of
 // every row (a ring of half rows), and the two CTAs add their row sums of g and g*xhat after
 // exchanging them through distributed shared memory (the same bits in both).

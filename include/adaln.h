@@ -78,7 +78,7 @@ typedef enum {
     ADALN_ERR_BAD_MOD_IDX = 7,  /* device data: mod_idx out of range (adaln_read_status) */
     ADALN_ERR_TIMEOUT = 8       /* a kernel gave up waiting (1 s) for a bulk copy of its
                                    input rows, or for the row sums of the other CTA of its
-                                   cluster (fp32 rows wider than 14456); its outputs from
+                                   cluster (fp32 rows wider than 14336); its outputs from
                                    then on are not valid (adaln_read_status) */
 } adaln_status;
 
@@ -98,7 +98,7 @@ size_t adaln_bwd_workspace_size(int64_t Bt, int64_t N, int64_t D, adaln_dtype dt
  * coalesced reduction"): each row's dx is computed from the saved statistics while threads
  * pinned to feature indices accumulate dy and dy*xhat down their tile of rows; per-tile
  * partials are summed by a second, fixed-order stage. Two launches on `stream`; for fp32
- * rows wider than 14456 the first is a launch of two-CTA thread-block clusters (each CTA
+ * rows wider than 14336 the first is a launch of two-CTA thread-block clusters (each CTA
  * half of every row), so such calls need a device and context that allow clusters. */
 int adaln_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
               const void* scale, void* dx, float* dshift, float* dscale, void* workspace,

@@ -95,6 +95,11 @@ SMALL = {
     "packed-f32-d15360-split": lambda: synth.make("c", 128, synth.F32, 15360, [700, 3, 0, 250, 47],
                                                   [1, 0, 2, 1, 1], 3, x_mode=synth.ROWS_SCALED,
                                                   dy_std=0.02),
+    # The narrowest split width: fp32 D=14344, half a row = 1793 vectors over 256 threads
+    # (eight a thread for 225 of them, the last with one).
+    "packed-f32-d14344-split-narrowest": lambda: synth.make("c", 129, synth.F32, 14344, [300, 1, 77],
+                                                            [0, 1, 0], 2, x_mode=synth.ROWS_SCALED,
+                                                            dy_std=0.02),
     "packed-f32-d128-many": lambda: synth.make(
         "c", 111, synth.F32, 128, list(np.random.default_rng(5).integers(0, 10, 100)),
         list(np.random.default_rng(6).integers(0, 13, 100)), 13),
