@@ -96,7 +96,7 @@ SMALL = {
                                                   [1, 0, 2, 1, 1], 3, x_mode=synth.ROWS_SCALED,
                                                   dy_std=0.02),
     # The narrowest split width: fp32 D=14344, half a row = 1793 vectors over 256 threads
-    # (eight a thread for 225 of them, the last with one).
+    # (thread t owns vectors t + 256k: eight for thread 0, seven for the others).
     "packed-f32-d14344-split-narrowest": lambda: synth.make("c", 129, synth.F32, 14344, [300, 1, 77],
                                                             [0, 1, 0], 2, x_mode=synth.ROWS_SCALED,
                                                             dy_std=0.02),
