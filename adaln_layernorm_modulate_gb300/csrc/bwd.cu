@@ -673,7 +673,11 @@ __global__ void __launch_bounds__(kStage2Threads, 4) stage2_kernel(const Stage2A
     const int64_t R = a.seg.R, G = a.G;
     const float4* P = reinterpret_cast<const float4*>(a.partials) + c4;
 
-    for (int64_t m = blockIdx.y; m < a.seg.nmod; m += gridDim.y) {
+    for (int64_t my = blockIdx.y; my < a.seg.nmod; my += gridDim.y) {
+        // Modulation rows last to first: in a batch of ascending segment lengths the rows
+        // with the most pieces come last, and this way their CTAs start in the first wave
+        // (the packed D=3072 workload: 26.7 -> 19 us).
+        const int64_t m = a.seg.nmod - 1 - my;
         float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
         int64_t J = 0;  // pieces of row m before the current list
 
